@@ -1,0 +1,211 @@
+"""GPU parity through the C-ABI: the CUDA path against the oracle on the same
+seeded inputs.  Routing, permutation and quantised codes bit-exact; layer
+outputs within max-over-tokens ||y - y_ref||_inf / ||y_ref||_inf <= 1e-2."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _rel_err(y, ref):
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    num = np.abs(y - ref).max(axis=1)
+    den = np.abs(ref).max(axis=1)
+    return float((num / np.maximum(den, 1e-30)).max())
+
+
+def _bf16_bits_to_f64(t):
+    return oracle.bf16_to_f32(t.view(_torch().int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+
+
+def _oracle_expert(wl, layer, e):
+    codes, scales = [], []
+    for m in range(3):
+        c, s = oracle.quantize(W.expert_master(wl, layer, e, m), wl.bits, wl.group, wl.scale_dtype)
+        codes.append(c)
+        scales.append(s)
+    return oracle.QuantExpert(codes, scales)
+
+
+def _run(plan, layer, x_bits, wl):
+    torch = _torch()
+    T = x_bits.shape[0]
+    x = torch.from_numpy(x_bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    E, k = wl.experts, wl.top_k
+    dbg = dict(logits=torch.empty(T, E, dtype=torch.float32, device="cuda"),
+               topk_idx=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+               topk_w=torch.empty(T, k, dtype=torch.float32, device="cuda"),
+               counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+               perm=torch.empty(T * k, dtype=torch.int32, device="cuda"),
+               inv=torch.empty(T * k, dtype=torch.int32, device="cuda"))
+    plan.forward(layer, x, y, dbg=dbg)
+    torch.cuda.synchronize()
+    return y, {k_: v.cpu().numpy() for k_, v in dbg.items()}
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = W.WORKLOADS["tiny"]
+    plan, info = harness.build_plan(wl)
+    experts = [_oracle_expert(wl, 0, e) for e in range(wl.experts)]
+    yield wl, plan, info, experts
+    plan.close()
+
+
+def test_quantiser_codes_bit_exact(tiny):
+    """The library's GPU quantiser and the oracle's produce the same codes and scales."""
+    wl, plan, info, experts = tiny
+    q = info["quantiser"]
+    for e in (0, 5, 15):
+        codes, scales = q.expert(0, e)
+        for m in range(3):
+            assert np.array_equal(codes[m].cpu().numpy(), experts[e].codes[m])
+            got = scales[m].cpu().contiguous().view(-1).numpy().view(experts[e].scales[m].dtype)
+            assert np.array_equal(got, experts[e].scales[m].ravel())
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
+def test_tiny_layer(tiny, T):
+    wl, plan, info, experts = tiny
+    wr, bias, _ = info["routers"][0]
+    x = W.tokens(wl, 100 + T, 0, T)
+    y, r = _run(plan, 0, x, wl)
+    ref = oracle.layer_forward(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                               wl.scale_dtype, x, wr, bias)
+    assert np.array_equal(r["logits"], ref["logits"])
+    assert np.array_equal(r["topk_idx"], ref["idx"])
+    np.testing.assert_allclose(r["topk_w"], ref["w"], rtol=2e-6, atol=1e-7)
+    assert np.array_equal(r["counts"], ref["counts"])
+    assert np.array_equal(r["offsets"], ref["offsets"])
+    assert np.array_equal(r["perm"], ref["perm"])
+    assert np.array_equal(r["inv"], ref["inv"])
+    assert _rel_err(_bf16_bits_to_f64(y), ref["y"]) <= TOL
+
+
+def test_empty_batch_is_a_noop(tiny):
+    torch = _torch()
+    wl, plan, _, _ = tiny
+    x = torch.empty(0, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    plan.forward(0, x, torch.empty_like(x))
+
+
+def test_host_buffer_forward_matches_device_forward(tiny):
+    torch = _torch()
+    wl, plan, info, _ = tiny
+    x = W.tokens(wl, 7, 0, 8)
+    y_dev, _ = _run(plan, 0, x, wl)
+    xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    plan.forward_host(0, xh, yh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y_dev.view(torch.int16).cpu())
+
+
+def test_placement_changes_no_output_bit():
+    """Same layer placed all-HBM, all-host and mixed: identical y bits."""
+    torch = _torch()
+    from moe_expert_layer_sorted_gb300 import RES_HBM, RES_HOST, Plan, harness
+    wl = W.WORKLOADS["tiny"]
+    q = harness.ExpertQuantiser(wl)
+    wr, bias, _ = W.router(wl, 0)
+    x = W.tokens(wl, 3, 0, 8)
+    outs = []
+    for mode in ("hbm", "host", "mixed"):
+        res = [RES_HBM if (mode == "hbm" or (mode == "mixed" and e % 2)) else RES_HOST
+               for e in range(wl.experts)]
+        n_hbm = sum(r == RES_HBM for r in res)
+        plan = Plan(num_layers=1, num_experts=wl.experts, hidden=wl.hidden, inter=wl.inter,
+                    top_k=wl.top_k, weight_bits=wl.bits, group_size=wl.group,
+                    scale_dtype=wl.scale_dtype, max_tokens=8, hbm_experts=n_hbm)
+        plan.set_router(0, wr, bias)
+        for e in range(wl.experts):
+            codes, scales = q.expert(0, e)
+            plan.place_experts(0, e, [(codes, scales)], [res[e]])
+        y, _ = _run(plan, 0, x, wl)
+        st = plan.stats(0)
+        assert st["hits"] + st["misses"] == st["accesses"]
+        if mode == "host":
+            assert st["hits"] == 0 and st["misses"] == st["accesses"] > 0
+        outs.append(y.view(torch.int16).cpu())
+        plan.close()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_invalid_calls_return_status(tiny):
+    torch = _torch()
+    from moe_expert_layer_sorted_gb300 import MoeError, Plan
+    wl, plan, _, _ = tiny
+    x = torch.zeros(9, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(MoeError) as ei:
+        plan.forward(0, x, torch.empty_like(x))          # T > max_tokens
+    assert ei.value.status == 1
+    with pytest.raises(MoeError) as ei:
+        plan.forward(1, x[:2], torch.empty_like(x[:2]))  # no such layer
+    assert ei.value.status == 1
+    p2 = Plan(num_layers=1, num_experts=16, hidden=256, inter=128, top_k=2, weight_bits=4,
+              group_size=32, scale_dtype=0, max_tokens=8, hbm_experts=16)
+    with pytest.raises(MoeError) as ei:
+        p2.forward(0, x[:2], torch.empty_like(x[:2]))    # experts not placed
+    assert ei.value.status == 5
+    p2.close()
+    with pytest.raises(MoeError) as ei:                  # far beyond HBM
+        Plan(num_layers=1, num_experts=4096, hidden=65536, inter=65536, top_k=2, weight_bits=4,
+             group_size=128, scale_dtype=1, max_tokens=8, hbm_experts=4096)
+    assert ei.value.status == 2
+
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = W.WORKLOADS["decode"]
+    plan, info = harness.build_plan(wl)
+    yield wl, plan, info
+    plan.close()
+
+
+@pytest.mark.parametrize("T", [1, 4, 6])
+def test_decode_layer_full_size(decode_layer, T):
+    """Decode layer at full size (H=4096, I=1024, E=384, int3): routing bit-exact
+    and outputs of every token against the oracle, over steps until a host-resident
+    expert has been read."""
+    wl, plan, info = decode_layer
+    wr, bias, _ = info["routers"][0]
+    cache = {}
+    st0 = plan.stats(0)
+    saw_host = False
+    for step in range(6):
+        x = W.tokens(wl, 1000 * T + step, 0, T)
+        y, r = _run(plan, 0, x, wl)
+        lg = oracle.router_logits(x, wr, bias)
+        idx, w = oracle.topk(lg, wl.top_k)
+        assert np.array_equal(r["logits"], lg)
+        assert np.array_equal(r["topk_idx"], idx)
+        np.testing.assert_allclose(r["topk_w"], w, rtol=2e-6, atol=1e-7)
+        counts, offsets, perm, inv = oracle.permute(idx, wl.experts)
+        assert np.array_equal(r["perm"], perm) and np.array_equal(r["offsets"], offsets)
+        for e in np.unique(idx):
+            if e not in cache:
+                cache[e] = _oracle_expert(wl, 0, int(e))
+        experts = [cache.get(e) for e in range(wl.experts)]
+        ref = oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                                          wl.scale_dtype, x, wr, bias, np.arange(T))
+        assert _rel_err(_bf16_bits_to_f64(y), ref) <= TOL
+        saw_host |= bool(set(np.unique(idx).tolist()) & info["host_sets"][0])
+        if saw_host and step >= 1:
+            break
+    st = plan.stats(0)
+    assert st["accesses"] - st0["accesses"] == st["hits"] - st0["hits"] + st["misses"] - st0["misses"]
