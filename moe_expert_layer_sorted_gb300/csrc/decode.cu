@@ -68,6 +68,9 @@ struct RouterArgs {
   int miss_cap;
   unsigned long long* stats;  // this layer's counters
   int64_t expert_bytes, router_bytes;
+  float* xsum;  // [T][H/G]: zcorr * (sum of x over each scale group), for the expert kernel
+  int group;
+  float zcorr;
   moe_routing_out dbg;
 };
 
@@ -140,6 +143,19 @@ router_decode_kernel(RouterArgs a) {
     }
   }
 
+  // scale-group sums of x for the expert kernel: pair q = (t, group), one warp each
+  {
+    const int ng = H / a.group, npairs = T * ng;
+    for (int q = blockIdx.x * kRouterWarps + warp; q < npairs; q += gridDim.x * kRouterWarps) {
+      const int t = q / ng, grp = q % ng;
+      float v = 0.f;
+      for (int i = lane; i < a.group; i += 32) v += bf16f(xs[t * H + grp * a.group + i]);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) a.xsum[q] = a.zcorr * v;
+    }
+  }
+
   // ---- grid-wide completion: the last CTA does the rest
   __shared__ unsigned s_last;
   __threadfence();
@@ -162,22 +178,32 @@ router_decode_kernel(RouterArgs a) {
     int li[kMaxTopK];
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) { lv[j] = -INFINITY; li[j] = 0x7fffffff; }
-    for (int ee = lane; ee < E; ee += 32) {
-      const float v = __ldcg(a.logits + t * E + ee);
-      // indices arrive ascending, so strict '>' keeps the lower index first on ties
-      if (v > lv[kMaxTopK - 1] || li[kMaxTopK - 1] == 0x7fffffff) {
-        float cv = v;
-        int ci = ee;
+    for (int base = 0; base < E; base += 32 * 16) {
+      float vb[16];  // one round trip for 16 logits per lane
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-          const bool better = (li[j] == 0x7fffffff) || (cv > lv[j]);
-          if (better) {
-            const float tv = lv[j];
-            const int ti = li[j];
-            lv[j] = cv;
-            li[j] = ci;
-            cv = tv;
-            ci = ti;
+      for (int q = 0; q < 16; ++q) {
+        const int ee = base + q * 32 + lane;
+        vb[q] = ee < E ? __ldcg(a.logits + t * E + ee) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int ee = base + q * 32 + lane;
+        const float v = vb[q];
+        // indices arrive ascending, so strict '>' keeps the lower index first on ties
+        if (ee < E && (v > lv[kMaxTopK - 1] || li[kMaxTopK - 1] == 0x7fffffff)) {
+          float cv = v;
+          int ci = ee;
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) {
+            const bool better = (li[j] == 0x7fffffff) || (cv > lv[j]);
+            if (better) {
+              const float tv = lv[j];
+              const int ti = li[j];
+              lv[j] = cv;
+              li[j] = ci;
+              cv = tv;
+              ci = ti;
+            }
           }
         }
       }
@@ -256,47 +282,68 @@ router_decode_kernel(RouterArgs a) {
   if (a.dbg.logits)
     for (int i = tid; i < T * E; i += blockDim.x) a.dbg.logits[i] = __ldcg(a.logits + i);
 
-  // distinct experts in ascending order; host-resident ones first
+  // distinct experts in ascending order, host-resident ones first: position p
+  // of perm starts a distinct expert when its expert differs from p-1's
+  __shared__ int s_first[kDecodeMaxTokens * kMaxTopK];  // 1 = HBM-first, 2 = host-first, 0 = not first
+  __shared__ const uint8_t* s_blob[kDecodeMaxTokens * kMaxTopK];
+  for (int p = tid; p < n; p += blockDim.x) {
+    const int ee = s_e[s_perm[p]];
+    int f = 0;
+    if (p == 0 || s_e[s_perm[p - 1]] != ee) {
+      const uint8_t* hb = a.blob_hbm[ee];
+      f = hb ? 1 : 2;
+      s_blob[p] = hb ? hb : a.blob_host[ee];
+    }
+    s_first[p] = f;
+  }
+  __syncthreads();
+  for (int p = tid; p < n; p += blockDim.x) {
+    const int f = s_first[p];
+    if (!f) continue;
+    int nh_all = 0, before = 0;
+    for (int q = 0; q < n; ++q) {
+      nh_all += s_first[q] == 2;
+      before += q < p && s_first[q] == f;
+    }
+    const int slot = f == 2 ? before : nh_all + before;
+    const int ee = s_e[s_perm[p]];
+    int cnt = 1;
+    while (p + cnt < n && s_first[p + cnt] == 0) ++cnt;
+    a.wl_expert[slot] = ee;
+    a.wl_off[slot] = p;
+    a.wl_cnt[slot] = cnt;
+    a.wl_blob[slot] = s_blob[p];
+    if (a.lfu) {  // distinct experts: no two threads touch the same g
+      const int64_t g = a.ge0 + ee;
+      a.lfu_count[g] += 1u;
+      a.lfu_last[g] = a.step;
+      if (f == 2) {
+        const unsigned mi = atomicAdd(a.miss_count, 1u);
+        if ((int)mi < a.miss_cap) a.miss_list[mi] = (int32_t)g;
+      }
+    }
+  }
   if (tid == 0) {
     int nd = 0, nh = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-      for (int p = 0; p < n; ++p) {
-        const int ee = s_e[s_perm[p]];
-        if (p > 0 && s_e[s_perm[p - 1]] == ee) continue;
-        int cnt = 1;
-        while (p + cnt < n && s_e[s_perm[p + cnt]] == ee) ++cnt;
-        const uint8_t* hb = a.blob_hbm[ee];
-        const bool host = hb == nullptr;
-        if ((pass == 0) != host) continue;
-        a.wl_expert[nd] = ee;
-        a.wl_off[nd] = p;
-        a.wl_cnt[nd] = cnt;
-        a.wl_blob[nd] = host ? a.blob_host[ee] : hb;
-        ++nd;
-        if (host) ++nh;
-        if (a.lfu) {
-          const int64_t g = a.ge0 + ee;
-          a.lfu_count[g] += 1u;
-          a.lfu_last[g] = a.step;
-          if (host) {
-            const unsigned mi = atomicAdd(a.miss_count, 1u);
-            if ((int)mi < a.miss_cap) a.miss_list[mi] = (int32_t)g;
-          }
-        }
-      }
+    for (int q = 0; q < n; ++q) {
+      nd += s_first[q] != 0;
+      nh += s_first[q] == 2;
     }
     s_nd = nd;
     a.ctl->ndistinct = nd;
     a.ctl->nhost = nh;
     a.ctl->queue = 0;
     unsigned long long* st = a.stats;
-    st[kStatAccesses] += nd;
-    st[kStatHits] += nd - nh;
-    st[kStatMisses] += nh;
-    st[kStatHbmBytes] += (unsigned long long)(nd - nh) * a.expert_bytes + a.router_bytes;
-    st[kStatHostBytes] += (unsigned long long)nh * a.expert_bytes;
-    st[kStatPairs] += n;
-    st[kStatForwards] += 1;
+    const unsigned long long v0 = st[kStatAccesses], v1 = st[kStatHits], v2 = st[kStatMisses],
+                             v3 = st[kStatHbmBytes], v4 = st[kStatHostBytes], v5 = st[kStatPairs],
+                             v6 = st[kStatForwards];
+    st[kStatAccesses] = v0 + nd;
+    st[kStatHits] = v1 + (nd - nh);
+    st[kStatMisses] = v2 + nh;
+    st[kStatHbmBytes] = v3 + (unsigned long long)(nd - nh) * a.expert_bytes + a.router_bytes;
+    st[kStatHostBytes] = v4 + (unsigned long long)nh * a.expert_bytes;
+    st[kStatPairs] = v5 + n;
+    st[kStatForwards] = v6 + 1;
   }
   __syncthreads();
   for (int i = tid; i < s_nd; i += blockDim.x) a.done_a[i] = 0;
@@ -338,7 +385,8 @@ struct ExpertArgs {
   uint16_t* y;
   MatOff m[3];
   int group, sdt;
-  float zcorr;  // 128 + 2^(b-1)
+  float zcorr;         // 128 + 2^(b-1)
+  const float* xsum;   // [T][H/G] from the router: zcorr * group sums of x
   uint32_t* err;
   int nA, nB;
 };
@@ -410,24 +458,23 @@ __device__ bool wait_count(const unsigned* ctr, unsigned target, uint32_t* err) 
 }
 
 // Group sums of the B operand rows: csum[g * 8 + t] = zcorr * sum_{k in group g} v_t[k]
-// for t < Te (0 for t >= Te); one warp per (group, token), fixed order.
+// for t < Te (entries for t >= Te are left unset and never used for an
+// output); one warp per (group, token), fixed order.
 __device__ void group_sums(const uint16_t* hi, const uint16_t* lo, int stride, int K, int G,
                            int Te, float zcorr, float* csum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = K / G;
-  for (int q = warp; q < ng * 8; q += kWarps) {
-    const int g = q >> 3, t = q & 7;
+  for (int q = warp; q < ng * Te; q += kWarps) {  // only real tokens; others are never read
+    const int g = q % ng, t = q / ng;
     float v = 0.f;
-    if (t < Te) {
-      for (int i = lane; i < G; i += 32) {
-        const int k = g * G + i;
-        v += bf16f(hi[t * stride + k]);
-        if (lo) v += bf16f(lo[t * stride + k]);
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int i = lane; i < G; i += 32) {
+      const int k = g * G + i;
+      v += bf16f(hi[t * stride + k]);
+      if (lo) v += bf16f(lo[t * stride + k]);
     }
-    if (lane == 0) csum[q] = zcorr * v;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) csum[g * 8 + t] = zcorr * v;
   }
 }
 
@@ -443,71 +490,79 @@ __device__ void a_unit(const ExpertArgs& a, int d, int mt, uint8_t* smem, const 
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   float* csum = reinterpret_cast<float*>(smem + (size_t)a.T * xstride * 2);
   float* red = csum + ng * 8;
+  float* ssc = red + kWarps * 256;  // [2][ng][16] gate / up scales of this row tile
   const uint8_t* blob = a.wl_blob[d];
+  const uint8_t* gb = blob + a.m[0].codes + (int64_t)mt * nkb * B * 512 + lane * 16;
+  const uint8_t* ub = blob + a.m[1].codes + (int64_t)mt * nkb * B * 512 + lane * 16;
+  const int gpb = kBlockK / G;  // scale groups per block
+  // two column blocks of this warp are in flight before x and the scales are
+  // staged; the loop keeps two in flight (one body copy, rotating buffers)
+  uint4 cg_[B], cu_[B], ng_[B], nu_[B];
+  auto load = [&](uint4(&pg)[B], uint4(&pu)[B], int kb) {
+    if (kb < nkb) {
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        pg[q] = ld_stream(gb + ((int64_t)kb * B + q) * 512);
+        pu[q] = ld_stream(ub + ((int64_t)kb * B + q) * 512);
+      }
+    }
+  };
+  load(cg_, cu_, warp);
+  load(ng_, nu_, warp + kWarps);
+  for (int i = tid; i < 2 * ng * kTileRows; i += blockDim.x) {
+    const int m = i / (ng * kTileRows), j = i % (ng * kTileRows);
+    ssc[i] = ld_scale(blob + a.m[m].scales, (int64_t)mt * ng * kTileRows + j, a.sdt);
+  }
   for (int i = tid; i < Te * (H / 8); i += blockDim.x) {
     const int t = i / (H / 8), c = i % (H / 8);
     *reinterpret_cast<uint4*>(xs + t * xstride + c * 8) =
         *reinterpret_cast<const uint4*>(a.x + (int64_t)toks[t] * H + c * 8);
   }
-  __syncthreads();
-  group_sums(xs, nullptr, xstride, H, G, Te, a.zcorr, csum);
+  for (int i = tid; i < ng * Te; i += blockDim.x) {
+    const int grp = i % ng, t = i / ng;
+    csum[grp * 8 + t] = __ldcg(a.xsum + (int64_t)toks[t] * ng + grp);
+  }
   __syncthreads();
 
-  const uint8_t* gb = blob + a.m[0].codes + (int64_t)mt * nkb * B * 512 + lane * 16;
-  const uint8_t* ub = blob + a.m[1].codes + (int64_t)mt * nkb * B * 512 + lane * 16;
-  const uint8_t* gs = blob + a.m[0].scales;
-  const uint8_t* us = blob + a.m[1].scales;
   const bool tv = g < Te;  // this lane's B-operand column is a real token
   const uint16_t* xrow = xs + g * xstride + 2 * tig;
   float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
-  constexpr int kR = B == 4 ? 1 : 2;  // column blocks in flight per warp (register budget)
-  for (int kb0 = warp; kb0 < nkb; kb0 += kR * kWarps) {
-    uint4 pg[kR][B], pu[kR][B];
+#pragma unroll 1
+  for (int kb = warp; kb < nkb; kb += kWarps) {
+    uint32_t wg[4 * B], wu[4 * B];
+    words_of<B>(cg_, wg);
+    words_of<B>(cu_, wu);
 #pragma unroll
-    for (int h = 0; h < kR; ++h) {
-      const int kb = kb0 + h * kWarps;
-      if (kb < nkb) {
-#pragma unroll
-        for (int q = 0; q < B; ++q) {
-          pg[h][q] = ld_stream(gb + ((int64_t)kb * B + q) * 512);
-          pu[h][q] = ld_stream(ub + ((int64_t)kb * B + q) * 512);
-        }
-      }
+    for (int q = 0; q < B; ++q) {
+      cg_[q] = ng_[q];
+      cu_[q] = nu_[q];
     }
+    load(ng_, nu_, kb + 2 * kWarps);
+    float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int h = 0; h < kR; ++h) {
-      const int kb = kb0 + h * kWarps;
-      if (kb >= nkb) break;
-      uint32_t wg[4 * B], wu[4 * B];
-      words_of<B>(pg[h], wg);
-      words_of<B>(pu[h], wu);
-      float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kt = 0; kt < 16; ++kt) {
+      const int k0 = kb * kBlockK + kt * 16;
+      const uint32_t b0 = tv ? *reinterpret_cast<const uint32_t*>(xrow + k0) : 0u;
+      const uint32_t b1 = tv ? *reinterpret_cast<const uint32_t*>(xrow + k0 + 8) : 0u;
+      mma_bf16(cg, pair_bits<B>(wg, 4 * kt), pair_bits<B>(wg, 4 * kt + 1),
+               pair_bits<B>(wg, 4 * kt + 2), pair_bits<B>(wg, 4 * kt + 3), b0, b1);
+      mma_bf16(cu, pair_bits<B>(wu, 4 * kt), pair_bits<B>(wu, 4 * kt + 1),
+               pair_bits<B>(wu, 4 * kt + 2), pair_bits<B>(wu, 4 * kt + 3), b0, b1);
+      if (((kt + 1) * 16) % G == 0) {  // end of a scale group
+        const int grp = kb * gpb + ((kt + 1) * 16) / G - 1;
+        const float* sg = ssc + grp * kTileRows + g;
+        const float* su = sg + ng * kTileRows;
+        const float z0 = csum[grp * 8 + 2 * tig], z1 = csum[grp * 8 + 2 * tig + 1];
+        accg[0] = fmaf(sg[0], cg[0] - z0, accg[0]);
+        accg[1] = fmaf(sg[0], cg[1] - z1, accg[1]);
+        accg[2] = fmaf(sg[8], cg[2] - z0, accg[2]);
+        accg[3] = fmaf(sg[8], cg[3] - z1, accg[3]);
+        accu[0] = fmaf(su[0], cu[0] - z0, accu[0]);
+        accu[1] = fmaf(su[0], cu[1] - z1, accu[1]);
+        accu[2] = fmaf(su[8], cu[2] - z0, accu[2]);
+        accu[3] = fmaf(su[8], cu[3] - z1, accu[3]);
 #pragma unroll
-      for (int kt = 0; kt < 16; ++kt) {
-        const int k0 = kb * kBlockK + kt * 16;
-        const uint32_t b0 = tv ? *reinterpret_cast<const uint32_t*>(xrow + k0) : 0u;
-        const uint32_t b1 = tv ? *reinterpret_cast<const uint32_t*>(xrow + k0 + 8) : 0u;
-        mma_bf16(cg, pair_bits<B>(wg, 4 * kt), pair_bits<B>(wg, 4 * kt + 1),
-                 pair_bits<B>(wg, 4 * kt + 2), pair_bits<B>(wg, 4 * kt + 3), b0, b1);
-        mma_bf16(cu, pair_bits<B>(wu, 4 * kt), pair_bits<B>(wu, 4 * kt + 1),
-                 pair_bits<B>(wu, 4 * kt + 2), pair_bits<B>(wu, 4 * kt + 3), b0, b1);
-        if (((kt + 1) * 16) % G == 0) {  // end of a scale group
-          const int grp = (k0 + 16 - G) / G;
-          const int64_t si = ((int64_t)mt * ng + grp) * kTileRows + g;
-          const float sg0 = ld_scale(gs, si, a.sdt), sg1 = ld_scale(gs, si + 8, a.sdt);
-          const float su0 = ld_scale(us, si, a.sdt), su1 = ld_scale(us, si + 8, a.sdt);
-          const float z0 = csum[grp * 8 + 2 * tig], z1 = csum[grp * 8 + 2 * tig + 1];
-          accg[0] = fmaf(sg0, cg[0] - z0, accg[0]);
-          accg[1] = fmaf(sg0, cg[1] - z1, accg[1]);
-          accg[2] = fmaf(sg1, cg[2] - z0, accg[2]);
-          accg[3] = fmaf(sg1, cg[3] - z1, accg[3]);
-          accu[0] = fmaf(su0, cu[0] - z0, accu[0]);
-          accu[1] = fmaf(su0, cu[1] - z1, accu[1]);
-          accu[2] = fmaf(su1, cu[2] - z0, accu[2]);
-          accu[3] = fmaf(su1, cu[3] - z1, accu[3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) cg[i] = cu[i] = 0.f;
-        }
+        for (int i = 0; i < 4; ++i) cg[i] = cu[i] = 0.f;
       }
     }
   }
@@ -552,18 +607,29 @@ __device__ bool b_unit(const ExpertArgs& a, int d, int ub, uint8_t* smem, const 
   uint16_t* hh = reinterpret_cast<uint16_t*>(smem);
   uint16_t* hl = hh + (size_t)a.T * hstride;
   float* csum = reinterpret_cast<float*>(hl + (size_t)a.T * hstride);
+  float* ssc = csum + ng * 8;  // [8 row tiles][ng][16] scales of this unit
   const int mtg = ub * (kBRows / kTileRows) + warp;
   const uint8_t* blob = a.wl_blob[d];
   const uint8_t* db = blob + a.m[2].codes + (int64_t)mtg * nkb * B * 512 + lane * 16;
   const uint8_t* ds = blob + a.m[2].scales;
-  constexpr int kPre = 4;  // column blocks loaded before the wait
-  uint4 pre[kPre][B];
+  constexpr int kPre = 4;  // column blocks loaded before the wait, then kept in flight
+  const int gpb = kBlockK / G;
+  uint4 q0[B], q1[B], q2[B], q3[B];
+  auto load = [&](uint4(&p)[B], int kb) {
+    if (kb < nkb) {
 #pragma unroll
-  for (int j = 0; j < kPre; ++j)
-    if (j < nkb) {
-#pragma unroll
-      for (int q = 0; q < B; ++q) pre[j][q] = ld_stream(db + ((int64_t)j * B + q) * 512);
+      for (int q = 0; q < B; ++q) p[q] = ld_stream(db + ((int64_t)kb * B + q) * 512);
     }
+  };
+  load(q0, 0);
+  load(q1, 1);
+  load(q2, 2);
+  load(q3, 3);
+  {
+    const int64_t s0 = (int64_t)ub * (kBRows / kTileRows) * ng * kTileRows;
+    for (int i = tid; i < (kBRows / kTileRows) * ng * kTileRows; i += blockDim.x)
+      ssc[i] = ld_scale(ds, s0 + i, a.sdt);
+  }
   if (tid == 0) *s_flag = wait_count(&a.done_a[d], (unsigned)a.nA, a.err) ? 1 : 0;
   __syncthreads();
   if (!*s_flag) return false;
@@ -582,9 +648,18 @@ __device__ bool b_unit(const ExpertArgs& a, int d, int ub, uint8_t* smem, const 
   const uint16_t* hrow = hh + g * hstride + 2 * tig;
   const uint16_t* lrow = hl + g * hstride + 2 * tig;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  auto block = [&](const uint4(&p)[B], int kb) {
+  const float* wsc = ssc + warp * ng * kTileRows + g;  // this warp's row tile, row g
+#pragma unroll 1
+  for (int kb = 0; kb < nkb; ++kb) {
     uint32_t w[4 * B];
-    words_of<B>(p, w);
+    words_of<B>(q0, w);
+#pragma unroll
+    for (int q = 0; q < B; ++q) {
+      q0[q] = q1[q];
+      q1[q] = q2[q];
+      q2[q] = q3[q];
+    }
+    load(q3, kb + kPre);
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kt = 0; kt < 16; ++kt) {
@@ -597,10 +672,9 @@ __device__ bool b_unit(const ExpertArgs& a, int d, int ub, uint8_t* smem, const 
       const uint32_t l1 = tv ? *reinterpret_cast<const uint32_t*>(lrow + k0 + 8) : 0u;
       mma_bf16(c, a0, a1, a2, a3, h0, h1);
       mma_bf16(c, a0, a1, a2, a3, l0, l1);
-      if (((kt + 1) * 16) % G == 0) {
-        const int grp = (k0 + 16 - G) / G;
-        const int64_t si = ((int64_t)mtg * ng + grp) * kTileRows + g;
-        const float s0 = ld_scale(ds, si, a.sdt), s1 = ld_scale(ds, si + 8, a.sdt);
+      if (((kt + 1) * 16) % G == 0) {  // end of a scale group
+        const int grp = kb * gpb + ((kt + 1) * 16) / G - 1;
+        const float s0 = wsc[grp * kTileRows], s1 = wsc[grp * kTileRows + 8];
         const float z0 = csum[grp * 8 + 2 * tig], z1 = csum[grp * 8 + 2 * tig + 1];
         acc[0] = fmaf(s0, c[0] - z0, acc[0]);
         acc[1] = fmaf(s0, c[1] - z1, acc[1]);
@@ -610,15 +684,6 @@ __device__ bool b_unit(const ExpertArgs& a, int d, int ub, uint8_t* smem, const 
         for (int i = 0; i < 4; ++i) c[i] = 0.f;
       }
     }
-  };
-#pragma unroll
-  for (int j = 0; j < kPre; ++j)
-    if (j < nkb) block(pre[j], j);
-  for (int kb = kPre; kb < nkb; ++kb) {
-    uint4 p[B];
-#pragma unroll
-    for (int q = 0; q < B; ++q) p[q] = ld_stream(db + ((int64_t)kb * B + q) * 512);
-    block(p, kb);
   }
   const int H = a.H;
 #pragma unroll
@@ -752,6 +817,9 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   r.stats = p.stats + (int64_t)layer * kNumStats;
   r.expert_bytes = p.lay.algo_bytes;
   r.router_bytes = (int64_t)E * H * 2;
+  r.xsum = p.xsum;
+  r.group = d.group_size;
+  r.zcorr = 128.0f + (float)(1 << (d.weight_bits - 1));
   if (dbg) r.dbg = *dbg;
   const int rgrid = (E + kRouterWarps - 1) / kRouterWarps;
   const size_t rsmem = (size_t)T * H * 2;
@@ -787,14 +855,15 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.group = d.group_size;
   a.sdt = d.scale_dtype;
   a.zcorr = 128.0f + (float)(1 << (d.weight_bits - 1));
+  a.xsum = p.xsum;
   a.err = p.err_dev;
   a.kpadI = p.lay.m[2].kpad;
   a.nA = I / kTileRows;
   a.nB = H / kBRows;
   const size_t smem_a = (size_t)T * (H + 8) * 2 + (size_t)(H / d.group_size) * 8 * 4 +
-                        (size_t)kWarps * 256 * 4;
-  const size_t smem_b =
-      (size_t)2 * T * (a.kpadI + 8) * 2 + (size_t)(a.kpadI / d.group_size) * 8 * 4;
+                        (size_t)kWarps * 256 * 4 + (size_t)2 * (H / d.group_size) * kTileRows * 4;
+  const size_t smem_b = (size_t)2 * T * (a.kpadI + 8) * 2 + (size_t)(a.kpadI / d.group_size) * 8 * 4 +
+                        (size_t)(kBRows / kTileRows) * (a.kpadI / d.group_size) * kTileRows * 4;
   const size_t smem = (std::max(smem_a, smem_b) + 15) / 16 * 16;
   const int maxD = std::min(E, T * k);
   const int units = maxD * (a.nA + a.nB);

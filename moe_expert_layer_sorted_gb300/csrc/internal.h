@@ -31,7 +31,7 @@ namespace moe {
 // group g (ngroups counts the padded K).
 constexpr int kTileRows = 16;
 constexpr int kBlockK = 256;
-constexpr int kBRows = 128;          // rows of the down projection per B work unit
+constexpr int kBRows = 64;           // rows of the down projection per B work unit
 constexpr int kDecodeMaxTokens = 8;  // forwards with T <= this use the decode path
 constexpr int kMaxTopK = 8;
 constexpr int kWarps = 8;            // warps per CTA of the decode expert kernel
@@ -110,8 +110,9 @@ struct Plan {
   unsigned* done_a = nullptr;         // [maxD]
   unsigned* done_b = nullptr;         // [H / kBRows]
   Ctl* ctl = nullptr;
-  float* hbuf = nullptr;        // [maxD][decode T][I] SwiGLU activations
+  float* hbuf = nullptr;        // [maxD][2][decode T][I] gate and up projections
   float* obuf = nullptr;        // [decode T * k][H] weighted expert outputs per slot
+  float* xsum = nullptr;        // [decode T][H / G] scale-group sums of the layer input
   uint16_t* x_stage = nullptr;  // [maxT][H] for the host-buffer forward
   uint16_t* y_stage = nullptr;
 

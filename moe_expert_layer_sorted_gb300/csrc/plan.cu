@@ -336,7 +336,7 @@ void release(Plan* p) {
   for (auto* b : p->bias) cudaFree(b);
   void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
-                 p->wl_blob, p->done_a, p->done_b, p->ctl, p->hbuf, p->obuf, p->x_stage,
+                 p->wl_blob, p->done_a, p->done_b, p->ctl, p->hbuf, p->obuf, p->xsum, p->x_stage,
                  p->y_stage, p->slot_of, p->slot_owner, p->lfu_count, p->lfu_last, p->miss_list,
                  p->miss_count, p->adm_list, p->adm_count, p->stats};
   for (void* v : dev)
@@ -390,7 +390,7 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
 
   // HBM need: arena + routers + tables + scratch, against free memory minus headroom
   const int64_t scratch = maxT * E * 4 + maxT * k * 16 + (E + 1) * 8 + maxD * 32 +
-                          maxD * decT * I * 4 + decT * k * H * 4 + 2 * maxT * H * 2 + 4096;
+                          2 * maxD * decT * I * 4 + decT * k * H * 4 + 2 * maxT * H * 2 + 4096;
   const int64_t lfu = d.cache_policy == MOE_POLICY_LFU
                           ? LE * 12 + slots * 8 + (int64_t)d.num_layers * maxD * 8
                           : 0;
@@ -463,8 +463,9 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   ALLOC(p->done_a, maxD);
   ALLOC(p->done_b, H / kBRows);
   ALLOC(p->ctl, 1);
-  ALLOC(p->hbuf, maxD * decT * I);
+  ALLOC(p->hbuf, 2 * maxD * decT * I);
   ALLOC(p->obuf, decT * k * H);
+  ALLOC(p->xsum, decT * (H / d.group_size));
   ALLOC(p->x_stage, maxT * H);
   ALLOC(p->y_stage, maxT * H);
   ALLOC(p->stats, (int64_t)d.num_layers * kNumStats);
