@@ -1,0 +1,339 @@
+"""Benchmark of the tiered MoE layer on GB300.
+
+Default workload: the decode MoE layer (H=4096, I=1024, E=384, top-6, int3
+G128 bf16 scales, Zipf(1.0) popularity, the 115 least popular experts in
+pinned host memory read over UVA).  One step = one forward at each decode
+batch size of that workload (T = 1, 4 and 6 tokens), with a fresh input per
+step; the metric is decode tokens/s over the step (11 tokens) and the
+weight-stream GB/s against the HBM + host-link roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Timing: CUDA events on the launching stream around
+each step (the step's forwards are one CUDA-graph replay); L2 is flushed
+(256 MiB write) between steps, outside the timed events.  `--impl reference`
+times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+BATCHES = (1, 4, 6)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(wl, tokens: int = 3, seed_base: int = 77):
+    """The oracle (single-threaded C, fp64 FFN) on `tokens` single-token
+    forwards of the workload: routing over the layer, then the routed experts
+    quantised, dequantised and evaluated.  Returns (tokens/s, seconds, sample)."""
+    import oracle
+    from synth import workloads as W
+    wr, bias, _ = W.router(wl, 0)
+    t0 = time.perf_counter()
+    for i in range(tokens):
+        x = W.tokens(wl, seed_base + i, 0, 1)
+        lg = oracle.router_logits(x, wr, bias)
+        idx, _ = oracle.topk(lg, wl.top_k)
+        experts = [None] * wl.experts
+        for e in np.unique(idx):
+            q = [oracle.quantize(W.expert_master(wl, 0, int(e), m), wl.bits, wl.group, wl.scale_dtype)
+                 for m in range(3)]
+            experts[int(e)] = oracle.QuantExpert([c for c, _ in q], [s for _, s in q])
+        oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                                    wl.scale_dtype, x, wr, bias, [0])
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt, f"{tokens} single-token forwards of the decode layer (routing + quantise + fp64 FFN of the routed experts)"
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from synth import workloads as W
+    wl = W.WORKLOADS["decode"]
+    import oracle
+    oracle.build()
+    import synth
+    synth.build()
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_baseline(wl, tokens=1, seed_base=10)
+    vals = []
+    total_tokens, total_s = 0, 0.0
+    for s in range(args.steps):
+        v, dt, sample = cpu_baseline(wl, tokens=1, seed_base=100 + s)
+        total_tokens += 1
+        total_s += dt
+    value = total_tokens / total_s
+    line = {"impl": "reference", "metric": "MoE decode tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode layer H=4096 I=1024 E=384 top-6 int3 G128 bf16 scales, "
+                                   "batch 1 (bounded CPU sample)"},
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": 1,
+                             "sample": f"{args.steps} single-token forwards"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from moe_expert_layer_sorted_gb300 import harness, probe_bandwidth
+    from synth import workloads as W
+
+    wl = W.WORKLOADS["decode"]
+    hbm_peak, peak_kind = _peaks()
+    link_gbs, hbm_probe = probe_bandwidth(local, 1 << 30, 5)
+    plan, info = harness.build_plan(wl, device=local)
+    stream = torch.cuda.Stream(dev)
+    H = wl.hidden
+    pool = 32
+    xs = {T: [torch.from_numpy(W.tokens(wl, 5000 + 97 * rank + s, 0, T).view(np.int16).copy())
+              .to(dev).view(torch.bfloat16) for s in range(pool)] for T in BATCHES}
+    ys = {T: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for T in BATCHES}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    with torch.cuda.stream(stream):
+        for T in BATCHES:  # first use sets the per-T launch configuration
+            plan.forward(0, xs[T][0], ys[T], stream=stream)
+    stream.synchronize()
+    graphs = []
+    use_graph = not args.no_graph
+    if use_graph:
+        for s in range(pool):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for T in BATCHES:
+                    plan.forward(0, xs[T][s], ys[T], stream=torch.cuda.current_stream())
+            graphs.append(g)
+
+    def step(s):
+        if use_graph:
+            graphs[s % pool].replay()
+        else:
+            for T in BATCHES:
+                plan.forward(0, xs[T][s % pool], ys[T], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for w in range(args.warmup):
+            flush.zero_()
+            step(w)
+    stream.synchronize()
+    plan.stats(0, reset=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    times = []
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step(args.warmup + i)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    ck = clocks.stop()
+    ms = [a.elapsed_time(b) for a, b in times]
+    ms_step = float(np.mean(ms))
+    st = plan.stats(0)
+    fw = max(st["forwards"], 1)
+    hbm_b = st["hbm_bytes"] / args.steps     # per step (3 forwards)
+    host_b = st["host_bytes"] / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens_step = sum(BATCHES)
+    value = ws * tokens_step / (ms_step * 1e-3)
+    achieved = (hbm_b + host_b) / (ms_step * 1e-3) / 1e9
+    roof_s = hbm_b / (hbm_peak * 1e9) + host_b / (link_gbs * 1e9)
+    eff_peak = (hbm_b + host_b) / roof_s / 1e9
+
+    # per batch size (separate timing of each forward, same protocol)
+    per_batch = {}
+    for T in BATCHES:
+        plan.stats(0, reset=True)
+        tt = []
+        with torch.cuda.stream(stream):
+            for i in range(16):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                plan.forward(0, xs[T][i % pool], ys[T], stream=stream)
+                b.record(stream)
+                tt.append((a, b))
+        torch.cuda.synchronize()
+        m = float(np.median([a.elapsed_time(b) for a, b in tt]))
+        s2 = plan.stats(0)
+        hb, ob = s2["hbm_bytes"] / 16, s2["host_bytes"] / 16
+        rt = hb / (hbm_peak * 1e9) + ob / (link_gbs * 1e9)
+        per_batch[str(T)] = {"tokens_per_s": T / (m * 1e-3), "us_per_forward": m * 1e3,
+                             "hbm_MB": hb / 1e6, "host_MB": ob / 1e6,
+                             "roofline_us": rt * 1e6, "roofline_frac": rt / (m * 1e-3)}
+
+    # end to end through the host-buffer entry point (pinned buffers, copies timed)
+    xh = {T: [xs[T][s].view(torch.int16).cpu().pin_memory() for s in range(4)] for T in BATCHES}
+    yh = {T: torch.empty(T, H, dtype=torch.int16).pin_memory() for T in BATCHES}
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(max(args.steps // 2, 4)):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for T in BATCHES:
+                plan.forward_host(0, xh[T][i % 4], yh[T], stream=stream)
+            b.record(stream)
+            b.synchronize()
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_step = float(np.mean(e2e_ms))
+    io_bytes = tokens_step * H * 2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        v, dt, sample = cpu_baseline(wl, tokens=args.cpu_tokens)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": "MoE decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; weights N(0,0.02) quantised by the library's GPU quantiser)",
+            "config": {"workload": "decode MoE layer: H=4096, I=1024, E=384, top-6, int3 G128 bf16 "
+                                   "scales, Zipf(1.0), 115 least-popular experts in pinned host "
+                                   "memory (UVA), 269 in HBM; step = forwards at T=1, 4, 6",
+                       "tokens_per_step": tokens_step, "l2": "256 MiB flush between steps, outside the timed events",
+                       "cuda_graph": use_graph, "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "weight_stream_GBps": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": eff_peak, "unit": "GB/s",
+                         "frac": achieved / eff_peak, "traffic": None,
+                         "kernel": "router_logits_kernel + expert_decode_kernel (one forward)",
+                         "peak_note": f"sum-form roofline: HBM {hbm_peak:.0f} GB/s ({peak_kind}, "
+                                      f"MEASURED_PEAKS.json) for HBM bytes + measured host link "
+                                      f"{link_gbs:.1f} GB/s for host bytes",
+                         "hbm_bytes_per_step": hbm_b, "host_bytes_per_step": host_b},
+            "per_batch": per_batch,
+            "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe},
+            "e2e": {"value": ws * tokens_step / (e2e_step * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
+            "gpu_launches": 2 * len(BATCHES) * args.steps,
+            "clocks": ck, "wall_s_timed": wall,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

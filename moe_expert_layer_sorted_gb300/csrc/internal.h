@@ -138,6 +138,14 @@ struct Plan {
   cudaStream_t last_stream = nullptr;
   bool have_last = false;
 
+  // decode launch configuration per batch size T (computed on first use)
+  struct DecodeCfg {
+    bool ready = false;
+    size_t smem = 0, rsmem = 0;
+    int grid = 0, slot_bytes = 0;
+  } dcfg[kDecodeMaxTokens + 1];
+  size_t dsmem_set = 0, rsmem_set = 0;  // largest max-dynamic-smem attributes set so far
+
   std::atomic<int> busy{0};
   std::string last_error;
 };
