@@ -206,6 +206,31 @@ moe_status moe_quantize(const float* w, int rows, int cols, int bits, int group,
 moe_status moe_probe_bandwidth(int device, size_t bytes, int iters, double* host_read_gbs,
                                double* hbm_read_gbs);
 
+/* Routing that allocates nothing.  The source pages have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory at the
+ * point where they route tokens -- for example a serving runtime that has
+ * already reserved nearly all of HBM for its own pools (so a cudaMalloc would
+ * fail or would have to come out of memory it manages), or code running where
+ * an allocation call is not permitted.  It computes the router logits of x
+ * [T][H] bf16 (device) against wr [E][H] bf16 (device), plus bias [E] fp32
+ * (device) or NULL, in the same fixed fp32 summation order as
+ * moe_layer_forward, and writes the top-k per token (logit descending, ties
+ * to the lower expert index) to topk_idx [T][k] int32 and the renormalised
+ * softmax weights to topk_w [T][k] fp32 (both device).  Work space for the
+ * logits is a fixed device array of 262,144 floats (1 MiB) that every GPU
+ * loading this library holds until the process exits; T * E above that is
+ * rejected with MOE_ERR_INVALID, as are H not a positive multiple of 256,
+ * k outside [1, min(E, 8)] and x or wr not 16-byte aligned.  The first call
+ * on a device looks up that array's device address (cudaGetSymbolAddress)
+ * with the device current; make that first call before any stream capture.
+ * All calls share the one array, so calls whose work overlaps on the GPU
+ * (different streams, or different host threads) race and give wrong
+ * results; order them on one stream.  Stream-ordered; T = 0 is a no-op.
+ * Calls no allocator (no cudaMalloc, cudaFree or library allocation). */
+moe_status moe_route_noalloc(const void* x_bf16, int T, int H, const void* wr_bf16,
+                             const float* bias, int E, int k, int32_t* topk_idx, float* topk_w,
+                             void* stream);
+
 const char* moe_status_string(moe_status s);
 /* Last error text of `plan` (or of the last call that had no plan, for NULL). */
 const char* moe_last_error(const moe_plan* plan);

@@ -27,7 +27,7 @@ POLICY_STATIC, POLICY_LFU = 0, 1
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_set_router", "moe_update_router_bias",
            "moe_place_experts", "moe_layer_forward", "moe_layer_forward_host", "moe_step_end",
            "moe_cache_stats", "moe_residence_table", "moe_quantize", "moe_probe_bandwidth",
-           "moe_status_string", "moe_last_error"]
+           "moe_route_noalloc", "moe_status_string", "moe_last_error"]
 
 _P = ctypes.c_void_p
 
@@ -90,6 +90,7 @@ def lib():
         L.moe_quantize.argtypes = [_P, i32, i32, i32, i32, i32, _P, _P, _P]
         L.moe_probe_bandwidth.argtypes = [i32, ctypes.c_size_t, i32, ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_double)]
+        L.moe_route_noalloc.argtypes = [_P, i32, i32, _P, _P, i32, i32, _P, _P, _P]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_status_string.argtypes = [i32]
         L.moe_last_error.restype = ctypes.c_char_p
@@ -225,3 +226,15 @@ def probe_bandwidth(device=0, nbytes=1 << 30, iters=5) -> tuple[float, float]:
     h, d = ctypes.c_double(0), ctypes.c_double(0)
     _check(lib().moe_probe_bandwidth(device, nbytes, iters, ctypes.byref(h), ctypes.byref(d)))
     return h.value, d.value
+
+
+def route_noalloc(x, wr, bias, k, topk_idx, topk_w, stream=None):
+    """Router logits + top-k without any allocation by the library (see
+    moe_route_noalloc in include/moe.h): all buffers are the caller's device
+    tensors; work space is a fixed device array inside the library."""
+    T, H = x.shape
+    E = wr.shape[0]
+    rc = lib().moe_route_noalloc(_addr(x), T, H, _addr(wr), _addr(bias), E, k, _addr(topk_idx),
+                                 _addr(topk_w), _stream(stream))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_route_noalloc rejected the call")
