@@ -52,6 +52,7 @@ namespace {
 
 constexpr int kRouterWarps = 4;
 constexpr int kSlots = 3;                               // cp.async ring depth, in units
+constexpr int kHostCtas = 16;  // CTAs given the host-resident experts' units (enough to fill the link)
 constexpr int kMaxSlots = kDecodeMaxTokens * kMaxTopK;  // (token, expert) pairs per forward
 
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
@@ -95,10 +96,23 @@ router_logits_kernel(RouterArgs a) {
 #pragma unroll
   for (int q = 0; q < 16; ++q)
     if (ev && q < nm) wv[q] = __ldg(w + q * 32 + lane);
-  {
+  {  // x -> shared memory, eight 16-byte loads in flight per thread
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
-    for (int i = tid; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
+    const int n = T * H / 8;
+    for (int i0 = 0; i0 < n; i0 += 8 * kRouterWarps * 32) {
+      uint4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * kRouterWarps * 32 + tid;
+        if (i < n) v[q] = __ldg(src + i);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * kRouterWarps * 32 + tid;
+        if (i < n) dst[i] = v[q];
+      }
+    }
   }
   if (blockIdx.x == 0) {  // the expert kernel's counters start at zero
     for (int i = tid; i < a.nda; i += blockDim.x) a.done_a[i] = 0u;
@@ -224,37 +238,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// A chunk = 4 consecutive 16-column steps of a block = 16 pairs, which the
-// field placement stores in exactly B consecutive words of the lane (words
-// B*c .. B*c + B - 1 for chunk c).  chunk_pair is pair_bits restricted to
-// one chunk: P = 4 * (step within chunk) + fragment register.
-template <int B>
-__device__ __forceinline__ uint32_t chunk_pair(const uint32_t (&w)[B], int P) {
-  constexpr uint32_t kMagic = 0x43004300u;
-  if constexpr (B == 4) {
-    return ((w[P >> 2] >> (4 * (P & 3))) & 0x000F000Fu) | kMagic;
-  } else if constexpr (B == 2) {
-    return ((w[P >> 3] >> (2 * (P & 7))) & 0x00030003u) | kMagic;
-  } else {
-    if (P < 15) return ((w[P / 5] >> (3 * (P % 5))) & 0x00070007u) | kMagic;
-    return ((w[0] >> 15) & 0x00010001u) | ((w[1] >> 14) & 0x00020002u) |
-           ((w[2] >> 13) & 0x00040004u) | kMagic;
-  }
-}
-
-// The lane's B words of chunk c of column block kb of a row tile staged in
-// shared memory (word q of the block sits at piece q/4, offset (q%4)*4).
-template <int B>
-__device__ __forceinline__ void chunk_words(const uint8_t* tile, int kb, int c, int lane,
-                                            uint32_t (&w)[B]) {
-#pragma unroll
-  for (int i = 0; i < B; ++i) {
-    const int q = B * c + i;
-    w[i] = *reinterpret_cast<const uint32_t*>(tile + ((kb * B + (q >> 2)) * 512) + lane * 16 +
-                                              (q & 3) * 4);
-  }
-}
-
 __device__ bool wait_count(const unsigned* ctr, unsigned target, uint32_t* err) {
   // bounded spin: gives up after ~2^22 polls (well over a second) and latches an error
   for (uint32_t it = 0; it < (1u << 22); ++it) {
@@ -266,6 +249,94 @@ __device__ bool wait_count(const unsigned* ctr, unsigned target, uint32_t* err) 
   *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout;
   __threadfence_system();
   return false;
+}
+
+
+// (a & m) | c in one instruction.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+  return d;
+}
+
+// bf16x2 register (128 + u_lo, 128 + u_hi) of pair P (0..63) of a lane's
+// 256-column block held in w (its 4*B words); P is a compile-time constant
+// after unrolling.  Field placement: see repack_codes_kernel in plan.cu.
+template <int B>
+__device__ __forceinline__ uint32_t pair_of(const uint32_t (&w)[4 * B], int P) {
+  constexpr uint32_t kMagic = 0x43004300u;  // bf16 128.0 in both halves
+  if constexpr (B == 4) {
+    return and_or(w[P >> 2] >> (4 * (P & 3)), 0x000F000Fu, kMagic);
+  } else if constexpr (B == 2) {
+    return and_or(w[P >> 3] >> (2 * (P & 7)), 0x00030003u, kMagic);
+  } else {
+    const int t = P >> 4, m = P & 15;
+    if (m < 15) return and_or(w[3 * t + m / 5] >> (3 * (m % 5)), 0x00070007u, kMagic);
+    const uint32_t v = and_or(w[3 * t] >> 15, 0x00010001u, kMagic);
+    const uint32_t u = and_or(w[3 * t + 1] >> 14, 0x00020002u, v);
+    return and_or(w[3 * t + 2] >> 13, 0x00040004u, u);
+  }
+}
+
+// One 256-column block of a 16-row weight tile (codes at `tile`, the lane's
+// words at tile + q*512 + lane*16) against the lane's B-operand row `bh`
+// (and, with HILO, the low part `bl`): for every scale group of the block,
+// acc += s * (C_group - z), where s = sc[gi*16] (row g) / sc[gi*16 + 8]
+// (row g + 8) and z = z0[gi*9] / z1[gi*9] for the lane's two C columns.
+// Two accumulator chains per part (even / odd steps) keep MMAs in flight.
+template <int B, int G, bool HILO>
+__device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const uint16_t* bh,
+                                           const uint16_t* bl, const float* sc, const float* z0,
+                                           const float* z1, float (&acc)[4]) {
+  uint32_t w[4 * B];
+#pragma unroll
+  for (int q = 0; q < B; ++q) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + q * 512 + lane * 16);
+    w[4 * q + 0] = v.x;
+    w[4 * q + 1] = v.y;
+    w[4 * q + 2] = v.z;
+    w[4 * q + 3] = v.w;
+  }
+  float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+  float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr int kSteps = G / 16;
+#pragma unroll
+  for (int kt = 0; kt < 16; ++kt) {
+    const uint32_t a0 = pair_of<B>(w, 4 * kt), a1 = pair_of<B>(w, 4 * kt + 1);
+    const uint32_t a2 = pair_of<B>(w, 4 * kt + 2), a3 = pair_of<B>(w, 4 * kt + 3);
+    const uint32_t h0 = *reinterpret_cast<const uint32_t*>(bh + kt * 16);
+    const uint32_t h1 = *reinterpret_cast<const uint32_t*>(bh + kt * 16 + 8);
+    mma_bf16((kt & 1) ? e1 : e0, a0, a1, a2, a3, h0, h1);
+    if constexpr (HILO) {
+      const uint32_t l0 = *reinterpret_cast<const uint32_t*>(bl + kt * 16);
+      const uint32_t l1 = *reinterpret_cast<const uint32_t*>(bl + kt * 16 + 8);
+      mma_bf16((kt & 1) ? f1 : f0, a0, a1, a2, a3, l0, l1);
+    }
+    if ((kt + 1) % kSteps == 0) {  // end of scale group gi (folded at compile time)
+      const int gi = (kt + 1) / kSteps - 1;
+      const float s0 = sc[gi * 16], s1 = sc[gi * 16 + 8];
+      const float y0 = z0[gi * 9], y1 = z1[gi * 9];
+      float c[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) c[q] = HILO ? (e0[q] + e1[q]) + (f0[q] + f1[q]) : e0[q] + e1[q];
+      acc[0] = fmaf(s0, c[0] - y0, acc[0]);
+      acc[1] = fmaf(s0, c[1] - y1, acc[1]);
+      acc[2] = fmaf(s1, c[2] - y0, acc[2]);
+      acc[3] = fmaf(s1, c[3] - y1, acc[3]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) e0[q] = e1[q] = f0[q] = f1[q] = 0.f;
+    }
+  }
+}
+
+template <int B, bool HILO>
+__device__ __forceinline__ void tile_block_g(int G, const uint8_t* tile, int lane,
+                                             const uint16_t* bh, const uint16_t* bl,
+                                             const float* sc, const float* z0, const float* z1,
+                                             float (&acc)[4]) {
+  if (G == 128) tile_block<B, 128, HILO>(tile, lane, bh, bl, sc, z0, z1, acc);
+  else if (G == 64) tile_block<B, 64, HILO>(tile, lane, bh, bl, sc, z0, z1, acc);
+  else tile_block<B, 32, HILO>(tile, lane, bh, bl, sc, z0, z1, acc);
 }
 
 struct Routing {  // per-CTA copy of this forward's routing (shared memory)
@@ -294,33 +365,105 @@ expert_decode_kernel(ExpertArgs a) {
   const int ngH = H / G, ngI = KP / G, nkbH = H / kBlockK, nkbI = KP / kBlockK;
   const int xstride = H + 8, hstride = KP + 8;  // bf16 elements; pads spread rows over banks
   const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
-  const int gsh = 31 - __clz(G);          // G is a power of two (32, 64 or 128)
-  const int kpgm = (G >> 4) - 1;          // 16-column steps per scale group, minus one
+  const int gpb = kBlockK / G;  // scale groups per 256-column block
 
-  // shared memory carve-up (all offsets multiples of 16 bytes)
-  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);  // [T][H+8]
-  size_t off = ((size_t)T * xstride * 2 + 15) / 16 * 16;
-  float* csa = reinterpret_cast<float*>(sm + off);  // [ngH][8]
-  off += (size_t)ngH * 8 * 4;
+  // shared memory carve-up (all offsets multiples of 16 bytes).  Row T of xs
+  // and of hh / hl is all zeros: B-operand columns of absent tokens read it.
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);  // [T+1][H+8]
+  size_t off = ((size_t)(T + 1) * xstride * 2 + 15) / 16 * 16;
+  float* csa = reinterpret_cast<float*>(sm + off);  // [ngH][9], column 8 = 0
+  off += ((size_t)ngH * 9 * 4 + 15) / 16 * 16;
   uint8_t* ring = sm + off;  // kSlots units
   off += (size_t)kSlots * a.slot_bytes;
-  uint16_t* hh = reinterpret_cast<uint16_t*>(sm + off);  // [T][KP+8]
-  uint16_t* hl = hh + (size_t)T * hstride;               // [T][KP+8]
-  off += ((size_t)2 * T * hstride * 2 + 15) / 16 * 16;
-  float* csb = reinterpret_cast<float*>(sm + off);  // [ngI][8]
-  off += (size_t)ngI * 8 * 4;
+  uint16_t* hh = reinterpret_cast<uint16_t*>(sm + off);  // [T+1][KP+8]
+  uint16_t* hl = hh + (size_t)(T + 1) * hstride;         // [T+1][KP+8]
+  off += ((size_t)2 * (T + 1) * hstride * 2 + 15) / 16 * 16;
+  float* csb = reinterpret_cast<float*>(sm + off);  // [ngI][9], column 8 = 0
+  off += ((size_t)ngI * 9 * 4 + 15) / 16 * 16;
   float* red = reinterpret_cast<float*>(sm + off);  // [8][16][8]
+  off += (size_t)kWarps * 128 * 4;
+  float* sf = reinterpret_cast<float*>(sm + off);  // unit scales as fp32
+
+  for (int i = tid; i < xstride; i += blockDim.x) xs[(size_t)T * xstride + i] = 0;
+  for (int i = tid; i < hstride; i += blockDim.x) {
+    hh[(size_t)T * hstride + i] = 0;
+    hl[(size_t)T * hstride + i] = 0;
+  }
+  for (int i = tid; i < ngH; i += blockDim.x) csa[i * 9 + 8] = 0.f;
+  for (int i = tid; i < ngI; i += blockDim.x) csb[i * 9 + 8] = 0.f;
 
   // ---- the layer input is not produced by the router: stage it first
   for (int t = 0; t < T; ++t)
-    for (int c = tid; c < H / 8; c += blockDim.x)
-      *reinterpret_cast<uint4*>(xs + t * xstride + c * 8) =
-          *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + c * 8);
+    for (int c0 = 0; c0 < H / 8; c0 += 4 * kWarps * 32) {  // four 16-byte loads in flight
+      uint4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + q * kWarps * 32 + tid;
+        if (c < H / 8) v[q] = *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + c * 8);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + q * kWarps * 32 + tid;
+        if (c < H / 8) *reinterpret_cast<uint4*>(xs + t * xstride + c * 8) = v[q];
+      }
+    }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- top-k, one warp per token: each lane keeps its own best 8 (logit
-  // desc, index asc) over experts lane, lane+32, ...; then k rounds of warp argmax
-  if (warp < T) {
+  // ---- top-k, one warp per token.  E <= 512: every lane holds the logits of
+  // experts lane, lane+32, ...; each of the k rounds takes the lane's best
+  // untaken logit (lowest index among equals), then a warp max over an
+  // order-preserving integer key and a warp min over the index among the
+  // lanes that hold the max (ties -> lower expert index).
+  if (warp < T && E <= 32 * 16) {
+    const int t = warp;
+    float vb[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int ee = q * 32 + lane;
+      vb[q] = ee < E ? __ldcg(a.logits + t * E + ee) : 0.f;
+    }
+    uint32_t taken = 0u;
+    for (int j = 0; j < k; ++j) {
+      float bv = 0.f;
+      int bq = -1;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int ee = q * 32 + lane;
+        if (ee < E && !((taken >> q) & 1u) && (bq < 0 || vb[q] > bv)) {
+          bv = vb[q];
+          bq = q;
+        }
+      }
+      uint32_t key = 0u;  // below every real key
+      if (bq >= 0) {
+        uint32_t ub = __float_as_uint(bv == 0.0f ? 0.0f : bv);  // -0 ties +0
+        key = (ub & 0x80000000u) ? ~ub : (ub | 0x80000000u);
+      }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t mine = (bq >= 0 && key == kmax) ? (uint32_t)(bq * 32 + lane) : 0xffffffffu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, mine);
+      const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31u));
+      if (bq >= 0 && (uint32_t)(bq * 32 + lane) == win) taken |= 1u << bq;
+      if (lane == 0) {
+        R.e[t * k + j] = (int)win;
+        R.w[t * k + j] = wv;  // logit for now
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const float l0 = R.w[t * k];
+      float ex[kMaxTopK];
+      float z = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        ex[j] = expf(R.w[t * k + j] - l0);
+        z += ex[j];
+      }
+      for (int j = 0; j < k; ++j) R.w[t * k + j] = ex[j] / z;
+    }
+  }
+  // ---- larger E: each lane keeps its own best 8 (logit desc, index asc)
+  // over experts lane, lane+32, ...; then k rounds of warp argmax
+  if (warp < T && E > 32 * 16) {
     const int t = warp;
     float lv[kMaxTopK];
     int li[kMaxTopK];
@@ -397,7 +540,7 @@ expert_decode_kernel(ExpertArgs a) {
   }
   for (int i = tid; i < T * ngH; i += blockDim.x) {
     const int t = i / ngH, grp = i % ngH;
-    csa[grp * 8 + t] = __ldcg(a.xsum + i);
+    csa[grp * 9 + t] = __ldcg(a.xsum + i);
   }
   __syncthreads();
 
@@ -506,99 +649,106 @@ expert_decode_kernel(ExpertArgs a) {
   const int tilesI = I / kTileRows;
   const int nA = 2 * tilesI;  // (row tile, gate|up) per expert
   const int nB = H / kBRows;  // 64-row blocks of the down projection per expert
-  const int U = D * (nA + nB);
   const int64_t a_codes = (int64_t)kTileRows * H * B / 8;
   const int a_scales = ngH * kTileRows * ssz;
   const int64_t b_codes = (int64_t)kBRows * KP * B / 8;
   const int b_scales = (kBRows / kTileRows) * ngI * kTileRows * ssz;
 
-  auto issue = [&](int u, int slot) {
+  // Unit lists.  When some but not all routed experts are host-resident,
+  // the first Ch CTAs take the host experts' units and the others the HBM
+  // experts' units, so the slow link reads run alongside the HBM stream
+  // instead of holding every CTA's first slots.  Within each list all A
+  // units come before all B units (a B unit waits only on A units, which
+  // never wait), and every CTA of the grid is resident, so no wait can block
+  // the units it waits for.
+  const int nh = R.nh;
+  int Ch = 0;
+  if (nh > 0 && nh < D && gridDim.x >= 2)
+    Ch = min(kHostCtas, min(nh * (nA + nB), (int)gridDim.x / 2));
+  const bool hostcta = (int)blockIdx.x < Ch;
+  const int dlo = (Ch == 0 || hostcta) ? 0 : nh;
+  const int dn = Ch == 0 ? D : (hostcta ? nh : D - nh);
+  const int cidx = (Ch == 0 || hostcta) ? (int)blockIdx.x : (int)blockIdx.x - Ch;
+  const int cstride = Ch == 0 ? (int)gridDim.x : (hostcta ? Ch : (int)gridDim.x - Ch);
+  const int Ul = dn * (nA + nB);
+  // i-th unit of this CTA: expert d, A (row tile r>>1, matrix r&1) or B (row block r)
+  auto unit_of = [&](int i, int& d, int& r, bool& isA) -> bool {
+    const int v = cidx + i * cstride;
+    if (v >= Ul) return false;
+    if (v < dn * nA) {
+      isA = true;
+      d = dlo + v / nA;
+      r = v % nA;
+    } else {
+      isA = false;
+      const int w = v - dn * nA;
+      d = dlo + w / nB;
+      r = w % nB;
+    }
+    return true;
+  };
+
+  // warps 1..7 issue the copies; warp 0 never has copies in flight, so its
+  // fences (the signals below) do not wait for the prefetch of later units
+  auto issue = [&](int i, int slot) {
+    int d, r;
+    bool isA;
+    if (!unit_of(i, d, r, isA) || tid < 32) return;
     const uint8_t* src_c;
     const uint8_t* src_s;
     int nc, ns;
-    if (u < D * nA) {
-      const int d = u / nA, r = u % nA, mm = r & 1, mt = r >> 1;
-      const uint8_t* blob = R.wl_blob[d];
+    const uint8_t* blob = R.wl_blob[d];
+    if (isA) {
+      const int mm = r & 1, mt = r >> 1;
       src_c = blob + a.m[mm].codes + (int64_t)mt * a_codes;
       src_s = blob + a.m[mm].scales + (int64_t)mt * a_scales;
       nc = (int)(a_codes / 16);
       ns = a_scales / 16;
     } else {
-      const int v = u - D * nA, d = v / nB, rb = v % nB;
-      const uint8_t* blob = R.wl_blob[d];
-      src_c = blob + a.m[2].codes + (int64_t)rb * b_codes;
-      src_s = blob + a.m[2].scales + (int64_t)rb * b_scales;
+      src_c = blob + a.m[2].codes + (int64_t)r * b_codes;
+      src_s = blob + a.m[2].scales + (int64_t)r * b_scales;
       nc = (int)(b_codes / 16);
       ns = b_scales / 16;
     }
     uint8_t* dst = ring + (size_t)slot * a.slot_bytes;
-    for (int c = tid; c < nc; c += blockDim.x) cp_async16(dst + c * 16, src_c + c * 16);
+    const int nthr = blockDim.x - 32;
+    for (int c = tid - 32; c < nc; c += nthr) cp_async16(dst + c * 16, src_c + c * 16);
     uint8_t* dsts = dst + (size_t)nc * 16;
-    for (int c = tid; c < ns; c += blockDim.x) cp_async16(dsts + c * 16, src_s + c * 16);
+    for (int c = tid - 32; c < ns; c += nthr) cp_async16(dsts + c * 16, src_s + c * 16);
   };
 
-  const int Gc = gridDim.x;
 #pragma unroll
   for (int i = 0; i < kSlots - 1; ++i) {
-    const int u = blockIdx.x + i * Gc;
-    if (u < U) issue(u, i);
+    issue(i, i);
     cp_async_commit();
   }
   for (int i = 0;; ++i) {
-    const int u = blockIdx.x + i * Gc;
-    if (u >= U) break;
-    {
-      const int un = blockIdx.x + (i + kSlots - 1) * Gc;
-      if (un < U) issue(un, (i + kSlots - 1) % kSlots);
-      cp_async_commit();
-    }
+    int d, r;
+    bool isA;
+    if (!unit_of(i, d, r, isA)) break;
+    issue(i + kSlots - 1, (i + kSlots - 1) % kSlots);
+    cp_async_commit();
     cp_async_wait<kSlots - 1>();
     __syncthreads();
     const uint8_t* slot = ring + (size_t)(i % kSlots) * a.slot_bytes;
 
-    if (u < D * nA) {
+    if (isA) {
       // ------------------------------------------------ A unit
-      const int d = u / nA, r = u % nA, mm = r & 1, mt = r >> 1;
+      const int mm = r & 1, mt = r >> 1;
       const int Te = R.wl_cnt[d], poff = R.wl_off[d];
-      const int tg = g < Te ? R.perm[poff + g] / k : 0;  // token of this lane's B column
-      const int c0 = 2 * tig, c1 = 2 * tig + 1;           // C columns (token slots) of this lane
-      const int tc0 = c0 < Te ? R.perm[poff + c0] / k : -1;
-      const int tc1 = c1 < Te ? R.perm[poff + c1] / k : -1;
-      const bool tv = g < Te;
-      const uint16_t* xrow = xs + tg * xstride + 2 * tig;
-      const uint8_t* sc = slot + a_codes;
+      const int c0 = 2 * tig, c1 = 2 * tig + 1;  // C columns (token slots) of this lane
+      const int tg = g < Te ? R.perm[poff + g] / k : T;  // B column g: its token, or the zero row
+      const int z0i = c0 < Te ? R.perm[poff + c0] / k : 8;
+      const int z1i = c1 < Te ? R.perm[poff + c1] / k : 8;
+      for (int i = tid; i < ngH * kTileRows; i += blockDim.x) sf[i] = scale_at(slot + a_codes, i, a.sdt);
+      __syncthreads();
+      const uint16_t* xb = xs + (size_t)tg * xstride + 2 * tig;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd steps
 #pragma unroll 1
-      for (int kb = warp; kb < nkbH; kb += kWarps) {
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t w[B];
-          chunk_words<B>(slot, kb, ch, lane, w);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int kt = 4 * ch + j;
-            const int k0 = kb * kBlockK + kt * 16;
-            const uint32_t b0 = tv ? *reinterpret_cast<const uint32_t*>(xrow + k0) : 0u;
-            const uint32_t b1 = tv ? *reinterpret_cast<const uint32_t*>(xrow + k0 + 8) : 0u;
-            mma_bf16((j & 1) ? co : ce, chunk_pair<B>(w, 4 * j), chunk_pair<B>(w, 4 * j + 1),
-                     chunk_pair<B>(w, 4 * j + 2), chunk_pair<B>(w, 4 * j + 3), b0, b1);
-            if (((kt + 1) & kpgm) == 0) {  // end of a scale group
-              const int grp = (k0 + 16 - G) >> gsh;
-              const float s0 = scale_at(sc, grp * kTileRows + g, a.sdt);
-              const float s1 = scale_at(sc, grp * kTileRows + g + 8, a.sdt);
-              const float z0 = tc0 >= 0 ? csa[grp * 8 + tc0] : 0.f;
-              const float z1 = tc1 >= 0 ? csa[grp * 8 + tc1] : 0.f;
-              acc[0] = fmaf(s0, (ce[0] + co[0]) - z0, acc[0]);
-              acc[1] = fmaf(s0, (ce[1] + co[1]) - z1, acc[1]);
-              acc[2] = fmaf(s1, (ce[2] + co[2]) - z0, acc[2]);
-              acc[3] = fmaf(s1, (ce[3] + co[3]) - z1, acc[3]);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) ce[q] = co[q] = 0.f;
-            }
-          }
-        }
-      }
+      for (int kb = warp; kb < nkbH; kb += kWarps)
+        tile_block_g<B, false>(G, slot + (size_t)kb * B * 512, lane, xb + kb * kBlockK, nullptr,
+                               sf + kb * gpb * kTileRows + g, csa + kb * gpb * 9 + z0i,
+                               csa + kb * gpb * 9 + z1i, acc);
       float* rw = red + warp * 128;  // [row 16][col 8]
       rw[g * 8 + c0] = acc[0];
       rw[g * 8 + c1] = acc[1];
@@ -612,31 +762,44 @@ expert_decode_kernel(ExpertArgs a) {
 #pragma unroll
           for (int ww = 0; ww < kWarps; ++ww) v += red[ww * 128 + tid];
           a.gu[(((int64_t)d * 2 + mm) * a.tstride + col) * I + mt * kTileRows + row] = v;
-          __threadfence();
         }
       }
       __syncthreads();
-      if (tid == 0) atomicAdd(&a.done_a[d], 1u);
+      if (tid == 0) {  // release: the barrier above orders the CTA's stores before this fence
+        __threadfence();
+        atomicAdd(&a.done_a[d], 1u);
+      }
     } else {
       // ------------------------------------------------ B unit
-      const int v = u - D * nA, d = v / nB, rb = v % nB;
+      const int rb = r;
       const int Te = R.wl_cnt[d], poff = R.wl_off[d];
       if (tid == 0) R.flag = wait_count(&a.done_a[d], (unsigned)nA, a.err) ? 1 : 0;
       __syncthreads();
       if (R.flag) {
         // h = silu(g) * u for the expert's tokens, split into bf16 hi + lo
-        for (int j = 0; j < Te; ++j)
-        for (int kk = tid; kk < KP; kk += blockDim.x) {
-          float h = 0.f;
-          if (kk < I) {
-            const float gv = __ldcg(a.gu + (((int64_t)d * 2 + 0) * a.tstride + j) * I + kk);
-            const float uv = __ldcg(a.gu + (((int64_t)d * 2 + 1) * a.tstride + j) * I + kk);
-            h = gv / (1.0f + expf(-gv)) * uv;
+        for (int j = 0; j < Te; ++j) {
+          const float* gj = a.gu + (((int64_t)d * 2 + 0) * a.tstride + j) * I;
+          const float* uj = a.gu + (((int64_t)d * 2 + 1) * a.tstride + j) * I;
+          for (int k0 = 0; k0 < KP; k0 += 4 * kWarps * 32) {
+            float gv[4], uv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // all loads of the batch in flight at once
+              const int kk = k0 + q * kWarps * 32 + tid;
+              gv[q] = kk < I ? __ldcg(gj + kk) : 0.f;
+              uv[q] = kk < I ? __ldcg(uj + kk) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int kk = k0 + q * kWarps * 32 + tid;
+              if (kk < KP) {
+                const float h = gv[q] / (1.0f + expf(-gv[q])) * uv[q];
+                const __nv_bfloat16 vh = __float2bfloat16_rn(h);
+                const __nv_bfloat16 vl = __float2bfloat16_rn(h - __bfloat162float(vh));
+                hh[j * hstride + kk] = __bfloat16_as_ushort(vh);
+                hl[j * hstride + kk] = __bfloat16_as_ushort(vl);
+              }
+            }
           }
-          const __nv_bfloat16 vh = __float2bfloat16_rn(h);
-          const __nv_bfloat16 vl = __float2bfloat16_rn(h - __bfloat162float(vh));
-          hh[j * hstride + kk] = __bfloat16_as_ushort(vh);
-          hl[j * hstride + kk] = __bfloat16_as_ushort(vl);
         }
         __syncthreads();
         // scale-group sums of hi + lo, one warp per (group, token)
@@ -649,52 +812,24 @@ expert_decode_kernel(ExpertArgs a) {
           }
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
-          if (lane == 0) csb[grp * 8 + j] = a.zcorr * sv;
+          if (lane == 0) csb[grp * 9 + j] = a.zcorr * sv;
         }
+        for (int i = tid; i < (kBRows / kTileRows) * ngI * kTileRows; i += blockDim.x)
+          sf[i] = scale_at(slot + b_codes, i, a.sdt);
         __syncthreads();
         const int tl = warp & 3, kpar = warp >> 2;  // row tile within the block, column-block parity
-        const bool tv = g < Te;
         const int c0 = 2 * tig, c1 = 2 * tig + 1;
-        const uint16_t* hrow = hh + g * hstride + 2 * tig;
-        const uint16_t* lrow = hl + g * hstride + 2 * tig;
-        const uint8_t* tile = slot + (int64_t)tl * nkbI * B * 512;
-        const uint8_t* sc = slot + b_codes + tl * ngI * kTileRows * ssz;
+        const int hr = g < Te ? g : T;  // B column g: the expert's token slot g, or the zero row
+        const uint16_t* hb = hh + (size_t)hr * hstride + 2 * tig;
+        const uint16_t* lb = hl + (size_t)hr * hstride + 2 * tig;
+        const int z0i = c0 < Te ? c0 : 8, z1i = c1 < Te ? c1 : 8;
+        const uint8_t* tile = slot + (size_t)tl * nkbI * B * 512;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        float ch_[4] = {0.f, 0.f, 0.f, 0.f}, cl_[4] = {0.f, 0.f, 0.f, 0.f};  // hi / lo parts of h
 #pragma unroll 1
-        for (int kb = kpar; kb < nkbI; kb += 2) {
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t w[B];
-            chunk_words<B>(tile, kb, cc, lane, w);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int kt = 4 * cc + j;
-              const int k0 = kb * kBlockK + kt * 16;
-              const uint32_t a0 = chunk_pair<B>(w, 4 * j), a1 = chunk_pair<B>(w, 4 * j + 1);
-              const uint32_t a2 = chunk_pair<B>(w, 4 * j + 2), a3 = chunk_pair<B>(w, 4 * j + 3);
-              const uint32_t h0 = tv ? *reinterpret_cast<const uint32_t*>(hrow + k0) : 0u;
-              const uint32_t h1 = tv ? *reinterpret_cast<const uint32_t*>(hrow + k0 + 8) : 0u;
-              const uint32_t l0 = tv ? *reinterpret_cast<const uint32_t*>(lrow + k0) : 0u;
-              const uint32_t l1 = tv ? *reinterpret_cast<const uint32_t*>(lrow + k0 + 8) : 0u;
-              mma_bf16(ch_, a0, a1, a2, a3, h0, h1);
-              mma_bf16(cl_, a0, a1, a2, a3, l0, l1);
-              if (((kt + 1) & kpgm) == 0) {  // end of a scale group
-                const int grp = (k0 + 16 - G) >> gsh;
-                const float s0 = scale_at(sc, grp * kTileRows + g, a.sdt);
-                const float s1 = scale_at(sc, grp * kTileRows + g + 8, a.sdt);
-                const float z0 = c0 < Te ? csb[grp * 8 + c0] : 0.f;
-                const float z1 = c1 < Te ? csb[grp * 8 + c1] : 0.f;
-                acc[0] = fmaf(s0, (ch_[0] + cl_[0]) - z0, acc[0]);
-                acc[1] = fmaf(s0, (ch_[1] + cl_[1]) - z1, acc[1]);
-                acc[2] = fmaf(s1, (ch_[2] + cl_[2]) - z0, acc[2]);
-                acc[3] = fmaf(s1, (ch_[3] + cl_[3]) - z1, acc[3]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) ch_[q] = cl_[q] = 0.f;
-              }
-            }
-          }
-        }
+        for (int kb = kpar; kb < nkbI; kb += 2)
+          tile_block_g<B, true>(G, tile + (size_t)kb * B * 512, lane, hb + kb * kBlockK,
+                                lb + kb * kBlockK, sf + (tl * ngI + kb * gpb) * kTileRows + g,
+                                csb + kb * gpb * 9 + z0i, csb + kb * gpb * 9 + z1i, acc);
         float* rw = red + warp * 128;
         rw[g * 8 + c0] = acc[0];
         rw[g * 8 + c1] = acc[1];
@@ -708,18 +843,26 @@ expert_decode_kernel(ExpertArgs a) {
             const float o = red[t4 * 128 + r16 * 8 + col] + red[(t4 + 4) * 128 + r16 * 8 + col];
             const int s = R.perm[poff + col];
             a.obuf[(int64_t)s * H + rb * kBRows + row] = R.w[s] * o;
-            __threadfence();
           }
         }
         __syncthreads();
-        if (tid == 0) R.flag = (atomicAdd(&a.done_b[rb], 1u) == (unsigned)D - 1) ? 2 : 0;
+        if (tid == 0) {  // release our rows, acquire everyone else's if we are last
+          __threadfence();
+          R.flag = (atomicAdd(&a.done_b[rb], 1u) == (unsigned)D - 1) ? 2 : 0;
+          __threadfence();
+        }
         __syncthreads();
         if (R.flag == 2) {  // every expert's contribution to these rows is in: combine
-          __threadfence();
           for (int i = tid; i < T * kBRows; i += blockDim.x) {
             const int t = i / kBRows, row = rb * kBRows + i % kBRows;
+            float ov[kMaxTopK];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)  // all k loads in flight, then summed in j order
+              if (j < k) ov[j] = __ldcg(a.obuf + (int64_t)(t * k + j) * H + row);
             float o = 0.f;
-            for (int j = 0; j < k; ++j) o += __ldcg(a.obuf + (int64_t)(t * k + j) * H + row);
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+              if (j < k) o += ov[j];
             a.y[(int64_t)t * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
           }
         }
@@ -778,9 +921,11 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
     const size_t b_unit =
         (size_t)kBRows * KP * b / 8 + (size_t)(kBRows / kTileRows) * (KP / G) * kTileRows * ssz;
     cf.slot_bytes = (int)((std::max(a_unit, b_unit) + 127) / 128 * 128);
-    cf.smem = ((size_t)T * (H + 8) * 2 + 15) / 16 * 16 + (size_t)(H / G) * 8 * 4 +
-              (size_t)kSlots * cf.slot_bytes + ((size_t)2 * T * (KP + 8) * 2 + 15) / 16 * 16 +
-              (size_t)(KP / G) * 8 * 4 + (size_t)kWarps * 128 * 4;
+    const size_t ngH = H / G, ngI = KP / G;
+    cf.smem = ((size_t)(T + 1) * (H + 8) * 2 + 15) / 16 * 16 + (ngH * 9 * 4 + 15) / 16 * 16 +
+              (size_t)kSlots * cf.slot_bytes + ((size_t)2 * (T + 1) * (KP + 8) * 2 + 15) / 16 * 16 +
+              (ngI * 9 * 4 + 15) / 16 * 16 + (size_t)kWarps * 128 * 4 +
+              std::max(ngH, (size_t)(kBRows / kTileRows) * ngI) * kTileRows * 4;
     cf.rsmem = (size_t)T * H * 2;
     const void* kfn = b == 2   ? (const void*)expert_decode_kernel<2>
                       : b == 3 ? (const void*)expert_decode_kernel<3>
