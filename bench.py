@@ -42,29 +42,89 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clocks and clock-event (throttle) reasons sampled during the timed
+    region.  The timed region of a decode step is a few milliseconds, shorter
+    than nvidia-smi's sampling period, so the primary sampler is a thread that
+    polls NVML's read-only queries (libnvidia-ml, shipped with the driver)
+    about every millisecond; nvidia-smi -lms is the fallback."""
 
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, torch_device_index: int):
+        self.dev = torch_device_index
+        self.samples = []
         self.proc = None
-        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+        self.thread = None
+        self.nvml = None
+        self.max_mhz = None
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        pr = torch.cuda.get_device_properties(self.dev)
+        bus = getattr(pr, "pci_bus_id", None)
+        if bus is not None:
+            dom = getattr(pr, "pci_domain_id", 0)
+            dv = getattr(pr, "pci_device_id", 0)
+            busid = f"{dom:08x}:{bus:02x}:{dv:02x}.0".encode()
+            if L.nvmlDeviceGetHandleByPciBusId_v2(busid, ctypes.byref(h)) == 0:
+                return L, h
+        if L.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(h)) == 0:
+            return L, h
+        return None
 
     def start(self):
+        import ctypes
+        import threading
         try:
+            self.nvml = self._nvml_handle()
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            L, h = self.nvml
+            mx = ctypes.c_uint(0)
+            if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = mx.value
+            self.stop_flag = False
+
+            def poll():
+                clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+                while not self.stop_flag:
+                    if L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                            L.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                        self.samples.append((clk.value, rs.value))
+                    time.sleep(0.001)
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.thread.start()
+            return
+        try:
+            self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
     def stop(self) -> dict:
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            sm = [c for c, _ in self.samples]
+            reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "samples": len(sm), "source": "nvml", "reasons": reasons}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["no clock source"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -75,20 +135,20 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 6:
                 continue
             try:
                 sm.append(float(parts[0]))
                 smax.append(float(parts[1]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+            for n, v in zip(names, parts[2:6]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "source": "nvidia-smi", "reasons": sorted(reasons)}
 
 
 def _dist():

@@ -2,29 +2,39 @@
 //
 // 1. router_logits_kernel: fp32 router logits x.Wr^T (+ bias) in the fixed
 //    summation order below, one warp per expert, plus the scale-group sums of
-//    x used by the expert kernel.  All of a warp's router-weight loads are in
-//    flight at once.
+//    x used by the expert kernel; it also advances the forward's epoch.
 //
-// 2. expert_decode_kernel (programmatic dependent launch): a persistent grid
-//    sized to be co-resident.  Every CTA
+// 2. expert_decode_kernel (programmatic dependent launch): a persistent grid,
+//    one CTA of 16 warps per SM, all co-resident.  Every CTA
 //      - stages the T input rows before it waits for the router;
 //      - takes the top-k of every token itself (logit descending, ties to the
 //        lower expert index), the renormalised softmax weights, the grouping
 //        of (token, expert) pairs by expert and the residence of each distinct
-//        expert (an HBM slot, or pinned host memory read in place over UVA),
-//        so no CTA waits on a serial last-block phase; CTA 0 alone writes the
-//        routing outputs and the cache accounting;
-//      - then runs its share of the work units, assigned round robin:
-//          A unit (expert d, 16 rows of I, gate or up): that projection for
-//            the expert's tokens -> gu buffer;
-//          B unit (expert d, 64 rows of H): h = silu(g) * u, o = Wd h for those
-//            rows times the routing weight -> obuf[slot]; the last B unit of a
-//            row block sums each token's k slots (j ascending) into y (bf16).
-//        A units come first (host-resident experts first, so the slow link
-//        reads start earliest and overlap the HBM ones); a B unit waits
-//        (bounded) for its expert's A units.  Each unit's weights and scales
-//        (24 KB at the decode shape) stream through a ring of cp.async slots,
-//        so the next units' bytes are in flight while one is computed.
+//        expert (an HBM slot, or pinned host memory read in place over UVA);
+//        CTA 0 alone writes the routing outputs and the cache accounting;
+//      - then runs its share of the work:
+//          A task (expert d, 16 rows of I): gate and up projections of those
+//            rows for the expert's tokens, streamed as NP units (column
+//            ranges of both matrices); at the end h = silu(g) * u in bf16,
+//            published to the other CTAs with the sums of each 16 h values;
+//          B unit (expert d, 64 rows of H): o = Wd h for those rows times the
+//            routing weight -> obuf[slot]; the B unit of the last distinct
+//            expert of a row block then sums each token's k slots (j
+//            ascending) into y (bf16).
+//        A tasks are dealt round robin and come first; B units follow in
+//        contiguous runs (so a CTA stages an expert's h once for several
+//        units), balanced against the A work.  Each unit's weights and
+//        scales (25.6 KB at the decode shape) stream through a ring of
+//        cp.async slots, so the next units' bytes are in flight while one is
+//        computed.  When some routed experts are host-resident, a few CTAs
+//        take all of their work, so the slow link reads overlap the HBM ones.
+//
+// Hand-offs between CTAs carry no fences or counters: every published word is
+// 64 bits, payload in the low half and the forward's epoch in the high half,
+// written and read with single-copy-atomic relaxed accesses; a reader waits
+// (bounded) until the word carries the current epoch.  Work is ordered so
+// that a unit only waits on units that come before it in every CTA's list,
+// and all CTAs are resident, so every wait ends.
 //
 // The MoE layer is that of "763B MoE in two 96 GB cards" (section "Where the
 // VRAM gap comes from": per layer, a token is routed to k of E experts; the
@@ -39,7 +49,7 @@
 // sum (128 + u) x = sum q x + (128 + 2^(b-1)) sum x with q = u - 2^(b-1); the
 // second term is subtracted per scale group from the fp32 accumulator.  All
 // products are exact in fp32; accumulation is fp32.  The down projection
-// feeds h as two bf16 parts (hi + lo) so that it sees ~16 significant bits.
+// takes h rounded to bf16 (the layer output is bf16 as well).
 #include <stdio.h>
 
 #include <algorithm>
@@ -51,8 +61,8 @@ using namespace moe;
 namespace {
 
 constexpr int kRouterWarps = 4;
-constexpr int kSlots = 3;                               // cp.async ring depth, in units
-constexpr int kHostCtas = 16;  // CTAs given the host-resident experts' units (enough to fill the link)
+constexpr int kMaxRing = 8;                             // cp.async ring depth bound, in units
+constexpr int kHostCtasMin = 4, kHostCtasMax = 16;  // CTAs given the host-resident experts' work
 constexpr int kMaxSlots = kDecodeMaxTokens * kMaxTopK;  // (token, expert) pairs per forward
 
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
@@ -68,10 +78,7 @@ struct RouterArgs {
   float* xsum;    // [T][H/G]: zcorr * sum of x over each scale group
   int group;
   float zcorr;
-  unsigned* done_a;
-  int nda;
-  unsigned* done_b;
-  int ndb;
+  unsigned* epoch;  // advanced once per forward
 };
 
 // Logits in the fixed order: lane j accumulates, from +0, fmaf(x[i], w[i], acc)
@@ -114,9 +121,9 @@ router_logits_kernel(RouterArgs a) {
       }
     }
   }
-  if (blockIdx.x == 0) {  // the expert kernel's counters start at zero
-    for (int i = tid; i < a.nda; i += blockDim.x) a.done_a[i] = 0u;
-    for (int i = tid; i < a.ndb; i += blockDim.x) a.done_b[i] = 0u;
+  if (blockIdx.x == 0 && tid == 0) {  // a new epoch for this forward's hand-off words (never 0)
+    const unsigned ep = *a.epoch + 1u;
+    *a.epoch = ep ? ep : 1u;
   }
   __syncthreads();
 
@@ -199,24 +206,23 @@ struct ExpertArgs {
   int32_t* miss_list;
   unsigned* miss_count;
   int miss_cap;
-  unsigned* done_a;  // [maxD]
-  unsigned* done_b;  // [H / kBRows]
-  float* gu;         // [maxD][2][tstride][I]
+  const unsigned* epoch;
+  unsigned long long* hbuf;  // [maxD][tstride][kpadI/2] tagged bf16 pairs of h
+  unsigned long long* hsum;  // [maxD][tstride][kpadI/16] tagged fp32 sums of 16 h values
+  unsigned long long* obuf;  // [T*k][H] tagged fp32 weighted expert outputs
   int tstride;
-  float* obuf;  // [T*k][H]
   uint16_t* y;
   MatOff m[3];
   int group, sdt;
   float zcorr;  // 128 + 2^(b-1)
   uint32_t* err;
-  int slot_bytes;
+  int slot_bytes, nslots;
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -238,19 +244,94 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ bool wait_count(const unsigned* ctr, unsigned target, uint32_t* err) {
-  // bounded spin: gives up after ~2^22 polls (well over a second) and latches an error
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= target) return true;
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long tagged(uint32_t payload, uint32_t epoch) {
+  return (unsigned long long)payload | ((unsigned long long)epoch << 32);
+}
+
+// Payload of a hand-off word once it carries `epoch` (v = a first read of it).
+// Bounded: after ~2^22 polls (well over a second) it latches a timeout in the
+// plan's error word and returns 0, so the kernel always ends.
+__device__ __noinline__ uint32_t wait_tagged(const unsigned long long* p, unsigned long long v,
+                                             uint32_t epoch, uint32_t* err) {
+  for (uint32_t it = 0; (uint32_t)(v >> 32) != epoch; ++it) {
+    // give up at once if another wait of this forward already timed out
+    if ((it & 4095u) == 4095u && *reinterpret_cast<volatile uint32_t*>(err)) return 0u;
+    if (it >= (1u << 22)) {
+      *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout;
+      __threadfence_system();
+      return 0u;
+    }
     __nanosleep(it < 64 ? 32 : 256);
+    v = ld_relaxed_u64(p);
+  }
+  return (uint32_t)v;
+}
+__device__ __forceinline__ uint32_t payload_of(const unsigned long long* p, unsigned long long v,
+                                               uint32_t epoch, uint32_t* err) {
+  return (uint32_t)(v >> 32) == epoch ? (uint32_t)v : wait_tagged(p, v, epoch, err);
+}
+
+// ---- mbarrier-tracked ring slots.  Each slot has a "full" barrier (one
+// arrival per use: the producer's expect_tx for an HBM unit, whose bulk
+// copies complete the bytes; for a host unit, lane 0 after every producer
+// lane has tied its cp.async copies to the barrier) and an "empty" barrier
+// (one arrival per consumer warp once it no longer reads the slot).  Pinned
+// host memory is read with plain 16-byte cp.async, as everywhere else in
+// this library.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// this thread's earlier cp.async copies arrive on bar when they land (the
+// pending count is raised now, so the phase cannot complete before that)
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// barrier among the consumer warps only (the producer warp never joins it)
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
+// bytes (a multiple of 16, both addresses 16-byte aligned) HBM -> shared, completing on bar
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Bounded wait for phase `parity` of bar: ~2^20 tries with a 1 us suspend
+// hint; latches a timeout (and gives up at once once one is latched).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+  for (uint32_t it = 0; it < (1u << 20); ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 255u) == 255u && *reinterpret_cast<volatile uint32_t*>(err)) return false;
   }
   *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout;
   __threadfence_system();
   return false;
 }
-
 
 // (a & m) | c in one instruction.
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
@@ -279,14 +360,14 @@ __device__ __forceinline__ uint32_t pair_of(const uint32_t (&w)[4 * B], int P) {
 }
 
 // One 256-column block of a 16-row weight tile (codes at `tile`, the lane's
-// words at tile + q*512 + lane*16) against the lane's B-operand row `bh`
-// (and, with HILO, the low part `bl`): for every scale group of the block,
-// acc += s * (C_group - z), where s = sc[gi*16] (row g) / sc[gi*16 + 8]
-// (row g + 8) and z = z0[gi*9] / z1[gi*9] for the lane's two C columns.
-// Two accumulator chains per part (even / odd steps) keep MMAs in flight.
-template <int B, int G, bool HILO>
+// words at tile + q*512 + lane*16) against the lane's B-operand row `bh`: for
+// every scale group gi of the block, acc += s * (C_gi - z), where s is the
+// scale of the lane's row g (element si + gi*16 of `scb`) or row g + 8
+// (si + gi*16 + 8), and z = z0[gi*9] / z1[gi*9] for the lane's two C columns.
+// Two accumulator chains (even / odd steps) keep MMAs in flight.
+template <int B, int G>
 __device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const uint16_t* bh,
-                                           const uint16_t* bl, const float* sc, const float* z0,
+                                           const uint8_t* scb, int si, int sdt, const float* z0,
                                            const float* z1, float (&acc)[4]) {
   uint32_t w[4 * B];
 #pragma unroll
@@ -298,7 +379,6 @@ __device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const 
     w[4 * q + 3] = v.w;
   }
   float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-  float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
   constexpr int kSteps = G / 16;
 #pragma unroll
   for (int kt = 0; kt < 16; ++kt) {
@@ -307,42 +387,35 @@ __device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const 
     const uint32_t h0 = *reinterpret_cast<const uint32_t*>(bh + kt * 16);
     const uint32_t h1 = *reinterpret_cast<const uint32_t*>(bh + kt * 16 + 8);
     mma_bf16((kt & 1) ? e1 : e0, a0, a1, a2, a3, h0, h1);
-    if constexpr (HILO) {
-      const uint32_t l0 = *reinterpret_cast<const uint32_t*>(bl + kt * 16);
-      const uint32_t l1 = *reinterpret_cast<const uint32_t*>(bl + kt * 16 + 8);
-      mma_bf16((kt & 1) ? f1 : f0, a0, a1, a2, a3, l0, l1);
-    }
     if ((kt + 1) % kSteps == 0) {  // end of scale group gi (folded at compile time)
       const int gi = (kt + 1) / kSteps - 1;
-      const float s0 = sc[gi * 16], s1 = sc[gi * 16 + 8];
+      const float s0 = scale_at(scb, si + gi * 16, sdt), s1 = scale_at(scb, si + gi * 16 + 8, sdt);
       const float y0 = z0[gi * 9], y1 = z1[gi * 9];
-      float c[4];
+      acc[0] = fmaf(s0, (e0[0] + e1[0]) - y0, acc[0]);
+      acc[1] = fmaf(s0, (e0[1] + e1[1]) - y1, acc[1]);
+      acc[2] = fmaf(s1, (e0[2] + e1[2]) - y0, acc[2]);
+      acc[3] = fmaf(s1, (e0[3] + e1[3]) - y1, acc[3]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) c[q] = HILO ? (e0[q] + e1[q]) + (f0[q] + f1[q]) : e0[q] + e1[q];
-      acc[0] = fmaf(s0, c[0] - y0, acc[0]);
-      acc[1] = fmaf(s0, c[1] - y1, acc[1]);
-      acc[2] = fmaf(s1, c[2] - y0, acc[2]);
-      acc[3] = fmaf(s1, c[3] - y1, acc[3]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) e0[q] = e1[q] = f0[q] = f1[q] = 0.f;
+      for (int q = 0; q < 4; ++q) e0[q] = e1[q] = 0.f;
     }
   }
 }
 
-template <int B, bool HILO>
+template <int B>
 __device__ __forceinline__ void tile_block_g(int G, const uint8_t* tile, int lane,
-                                             const uint16_t* bh, const uint16_t* bl,
-                                             const float* sc, const float* z0, const float* z1,
+                                             const uint16_t* bh, const uint8_t* scb, int si,
+                                             int sdt, const float* z0, const float* z1,
                                              float (&acc)[4]) {
-  if (G == 128) tile_block<B, 128, HILO>(tile, lane, bh, bl, sc, z0, z1, acc);
-  else if (G == 64) tile_block<B, 64, HILO>(tile, lane, bh, bl, sc, z0, z1, acc);
-  else tile_block<B, 32, HILO>(tile, lane, bh, bl, sc, z0, z1, acc);
+  if (G == 128) tile_block<B, 128>(tile, lane, bh, scb, si, sdt, z0, z1, acc);
+  else if (G == 64) tile_block<B, 64>(tile, lane, bh, scb, si, sdt, z0, z1, acc);
+  else tile_block<B, 32>(tile, lane, bh, scb, si, sdt, z0, z1, acc);
 }
 
 struct Routing {  // per-CTA copy of this forward's routing (shared memory)
   int e[kMaxSlots];                   // expert of slot s = t*k + j
   float w[kMaxSlots];                 // renormalised weight of slot s
   int perm[kMaxSlots];                // slots ordered by (expert, token)
+  int ptok[kMaxSlots];                // token of perm[p]
   int rank[kMaxSlots];                // position of slot s in perm
   int first[kMaxSlots];               // perm position p starts a distinct expert: 1 = HBM, 2 = host
   const uint8_t* pblob[kMaxSlots];
@@ -355,10 +428,11 @@ struct Routing {  // per-CTA copy of this forward's routing (shared memory)
 };
 
 template <int B>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__((kWarps + 1) * 32, 1)
 expert_decode_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ Routing R;
+  __shared__ __align__(8) unsigned long long fullb[kMaxRing], emptyb[kMaxRing];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tig = lane & 3;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, KP = a.kpadI, G = a.group;
@@ -366,29 +440,25 @@ expert_decode_kernel(ExpertArgs a) {
   const int xstride = H + 8, hstride = KP + 8;  // bf16 elements; pads spread rows over banks
   const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
   const int gpb = kBlockK / G;  // scale groups per 256-column block
+  const int sdt = a.sdt;
 
-  // shared memory carve-up (all offsets multiples of 16 bytes).  Row T of xs
-  // and of hh / hl is all zeros: B-operand columns of absent tokens read it.
-  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);  // [T+1][H+8]
-  size_t off = ((size_t)(T + 1) * xstride * 2 + 15) / 16 * 16;
+  // shared memory carve-up (all offsets multiples of 16 bytes)
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);  // [T][H+8] layer input
+  size_t off = ((size_t)T * xstride * 2 + 15) / 16 * 16;
   float* csa = reinterpret_cast<float*>(sm + off);  // [ngH][9], column 8 = 0
   off += ((size_t)ngH * 9 * 4 + 15) / 16 * 16;
-  uint8_t* ring = sm + off;  // kSlots units
-  off += (size_t)kSlots * a.slot_bytes;
-  uint16_t* hh = reinterpret_cast<uint16_t*>(sm + off);  // [T+1][KP+8]
-  uint16_t* hl = hh + (size_t)(T + 1) * hstride;         // [T+1][KP+8]
-  off += ((size_t)2 * (T + 1) * hstride * 2 + 15) / 16 * 16;
+  uint16_t* hs = reinterpret_cast<uint16_t*>(sm + off);  // [T][KP+8] staged h of one expert
+  off += ((size_t)T * hstride * 2 + 15) / 16 * 16;
   float* csb = reinterpret_cast<float*>(sm + off);  // [ngI][9], column 8 = 0
   off += ((size_t)ngI * 9 * 4 + 15) / 16 * 16;
-  float* red = reinterpret_cast<float*>(sm + off);  // [8][16][8]
-  off += (size_t)kWarps * 128 * 4;
-  float* sf = reinterpret_cast<float*>(sm + off);  // unit scales as fp32
+  float* red = reinterpret_cast<float*>(sm + off);  // [2][kWarps][16][8] per-warp partials
+  off += (size_t)2 * kWarps * 128 * 4;
+  float* gus = reinterpret_cast<float*>(sm + off);  // [2][16][8] gate, up of an A task
+  off += 2 * 128 * 4;
+  uint16_t* hq = reinterpret_cast<uint16_t*>(sm + off);  // [8][16] bf16 h of an A task
+  off += 128 * 2;
+  uint8_t* ring = sm + off;  // a.nslots units
 
-  for (int i = tid; i < xstride; i += blockDim.x) xs[(size_t)T * xstride + i] = 0;
-  for (int i = tid; i < hstride; i += blockDim.x) {
-    hh[(size_t)T * hstride + i] = 0;
-    hl[(size_t)T * hstride + i] = 0;
-  }
   for (int i = tid; i < ngH; i += blockDim.x) csa[i * 9 + 8] = 0.f;
   for (int i = tid; i < ngI; i += blockDim.x) csb[i * 9 + 8] = 0.f;
 
@@ -552,6 +622,7 @@ expert_decode_kernel(ExpertArgs a) {
     for (int q = 0; q < n; ++q) r += (R.e[q] * T + q / k) < key;
     R.rank[s] = r;
     R.perm[r] = s;
+    R.ptok[r] = s / k;
   }
   __syncthreads();
   for (int p = tid; p < n; p += blockDim.x) {
@@ -645,239 +716,317 @@ expert_decode_kernel(ExpertArgs a) {
     }
   }
 
-  // ---- work units
+  // ---- work
+  const uint32_t epoch = *reinterpret_cast<const volatile unsigned*>(a.epoch);
   const int tilesI = I / kTileRows;
-  const int nA = 2 * tilesI;  // (row tile, gate|up) per expert
-  const int nB = H / kBRows;  // 64-row blocks of the down projection per expert
-  const int64_t a_codes = (int64_t)kTileRows * H * B / 8;
-  const int a_scales = ngH * kTileRows * ssz;
+  const int nB = H / kBRows;                      // 64-row blocks of the down projection
+  const int NP = (nkbH + 7) / 8;                  // units per A task
+  const int kbpp = (nkbH + NP - 1) / NP;          // column blocks per A unit (the last may have fewer)
   const int64_t b_codes = (int64_t)kBRows * KP * B / 8;
   const int b_scales = (kBRows / kTileRows) * ngI * kTileRows * ssz;
 
-  // Unit lists.  When some but not all routed experts are host-resident,
-  // the first Ch CTAs take the host experts' units and the others the HBM
-  // experts' units, so the slow link reads run alongside the HBM stream
-  // instead of holding every CTA's first slots.  Within each list all A
-  // units come before all B units (a B unit waits only on A units, which
-  // never wait), and every CTA of the grid is resident, so no wait can block
-  // the units it waits for.
+  // Work lists.  When some but not all routed experts are host-resident, the
+  // first Ch CTAs take the host experts' work and the others the HBM
+  // experts'.  In a list, A tasks are dealt round robin and every CTA runs
+  // its A tasks before its B units; B units, ordered by (expert, row block),
+  // are split into contiguous runs, CTAs with fewer A tasks first.  The
+  // combines of row blocks come last.  A B unit waits only on A tasks and a
+  // combine only on B units, so every wait is on work that some resident CTA
+  // runs before anything it could be blocked by.
   const int nh = R.nh;
   int Ch = 0;
-  if (nh > 0 && nh < D && gridDim.x >= 2)
-    Ch = min(kHostCtas, min(nh * (nA + nB), (int)gridDim.x / 2));
+  if (nh > 0 && nh < D && gridDim.x >= 2)  // the host share of the grid, within [4, 16] (4 fill the link)
+    Ch = min(min(kHostCtasMax, max(kHostCtasMin, ((int)gridDim.x * nh + D / 2) / D)),
+             min(nh * (tilesI + nB), (int)gridDim.x / 2));
   const bool hostcta = (int)blockIdx.x < Ch;
   const int dlo = (Ch == 0 || hostcta) ? 0 : nh;
   const int dn = Ch == 0 ? D : (hostcta ? nh : D - nh);
   const int cidx = (Ch == 0 || hostcta) ? (int)blockIdx.x : (int)blockIdx.x - Ch;
-  const int cstride = Ch == 0 ? (int)gridDim.x : (hostcta ? Ch : (int)gridDim.x - Ch);
-  const int Ul = dn * (nA + nB);
-  // i-th unit of this CTA: expert d, A (row tile r>>1, matrix r&1) or B (row block r)
-  auto unit_of = [&](int i, int& d, int& r, bool& isA) -> bool {
-    const int v = cidx + i * cstride;
-    if (v >= Ul) return false;
-    if (v < dn * nA) {
-      isA = true;
-      d = dlo + v / nA;
-      r = v % nA;
+  const int cs = Ch == 0 ? (int)gridDim.x : (hostcta ? Ch : (int)gridDim.x - Ch);
+  const int nAt = dn * tilesI, nBu = dn * nB;
+  const int nAc = cidx < nAt ? (nAt - 1 - cidx) / cs + 1 : 0;  // A tasks of this CTA
+  const int ord = (cidx - nAt % cs + cs) % cs;
+  const int bq = nBu / cs, br = nBu % cs;
+  const int nBc = bq + (ord < br ? 1 : 0);
+  const int blo = ord * bq + min(ord, br);
+  const int nU = nAc * NP + nBc;
+  // i-th unit of this CTA: expert d; A: row tile r, part pa; B: row block r
+  auto unit_of = [&](int i, int& d, int& r, int& pa) -> bool {
+    if (i < nAc * NP) {
+      const int task = cidx + (i / NP) * cs;
+      pa = i % NP;
+      d = dlo + task / tilesI;
+      r = task % tilesI;
     } else {
-      isA = false;
-      const int w = v - dn * nA;
-      d = dlo + w / nB;
-      r = w % nB;
+      const int v = blo + (i - nAc * NP);
+      pa = -1;
+      d = dlo + v / nB;
+      r = v % nB;
     }
     return true;
   };
 
-  // warps 1..7 issue the copies; warp 0 never has copies in flight, so its
-  // fences (the signals below) do not wait for the prefetch of later units
-  auto issue = [&](int i, int slot) {
-    int d, r;
-    bool isA;
-    if (!unit_of(i, d, r, isA) || tid < 32) return;
-    const uint8_t* src_c;
-    const uint8_t* src_s;
-    int nc, ns;
+  // Producer warp: unit i into ring slot `slot`.  hostmask bit s: the slot's
+  // previous unit was written by cp.async (then the bulk copy that reuses it
+  // is ordered after those writes by a proxy fence).
+  auto issue = [&](int i, int slot, uint32_t& hostmask) {
+    int d, r, pa;
+    unit_of(i, d, r, pa);
     const uint8_t* blob = R.wl_blob[d];
-    if (isA) {
-      const int mm = r & 1, mt = r >> 1;
-      src_c = blob + a.m[mm].codes + (int64_t)mt * a_codes;
-      src_s = blob + a.m[mm].scales + (int64_t)mt * a_scales;
-      nc = (int)(a_codes / 16);
-      ns = a_scales / 16;
-    } else {
-      src_c = blob + a.m[2].codes + (int64_t)r * b_codes;
-      src_s = blob + a.m[2].scales + (int64_t)r * b_scales;
-      nc = (int)(b_codes / 16);
-      ns = b_scales / 16;
-    }
     uint8_t* dst = ring + (size_t)slot * a.slot_bytes;
-    const int nthr = blockDim.x - 32;
-    for (int c = tid - 32; c < nc; c += nthr) cp_async16(dst + c * 16, src_c + c * 16);
-    uint8_t* dsts = dst + (size_t)nc * 16;
-    for (int c = tid - 32; c < ns; c += nthr) cp_async16(dsts + c * 16, src_s + c * 16);
+    const uint32_t bar = smem_addr(&fullb[slot]);
+    // segments: A = gate codes | up codes | gate scales | up scales of the
+    // column range; B = codes | scales of 4 row tiles of the down projection
+    const uint8_t* src[4];
+    uint32_t len[4];
+    int nseg;
+    if (pa >= 0) {
+      const int kb0 = pa * kbpp, nkp = min(nkbH, kb0 + kbpp) - kb0;
+      const int64_t co = ((int64_t)r * nkbH + kb0) * B * 512;
+      const int64_t so = ((int64_t)r * ngH + (int64_t)kb0 * gpb) * kTileRows * ssz;
+      src[0] = blob + a.m[0].codes + co;
+      src[1] = blob + a.m[1].codes + co;
+      src[2] = blob + a.m[0].scales + so;
+      src[3] = blob + a.m[1].scales + so;
+      len[0] = len[1] = (uint32_t)nkp * B * 512;
+      len[2] = len[3] = (uint32_t)(nkp * gpb * kTileRows * ssz);
+      nseg = 4;
+    } else {
+      src[0] = blob + a.m[2].codes + (int64_t)r * b_codes;
+      src[1] = blob + a.m[2].scales + (int64_t)r * b_scales;
+      len[0] = (uint32_t)b_codes;
+      len[1] = (uint32_t)b_scales;
+      len[2] = len[3] = 0;
+      nseg = 2;
+    }
+    if (d >= R.nh) {  // HBM-resident: lane 0's bulk copies
+      if (lane == 0) {
+        uint32_t tot = 0;
+        for (int q = 0; q < nseg; ++q) tot += len[q];
+        if ((hostmask >> slot) & 1u) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(bar, tot);
+        uint32_t o = 0;
+        for (int q = 0; q < nseg; ++q) {
+          bulk_g2s(smem_addr(dst + o), src[q], len[q], bar);
+          o += len[q];
+        }
+      }
+      hostmask &= ~(1u << slot);
+    } else {  // pinned host memory: 16-byte cp.async by the producer's lanes
+      uint32_t o = 0;
+      for (int q = 0; q < nseg; ++q) {
+        for (uint32_t c = lane; c < len[q] / 16; c += 32) cp_async16(dst + o + c * 16, src[q] + c * 16);
+        o += len[q];
+      }
+      cp_async_mbar_arrive(bar);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+      hostmask |= 1u << slot;
+    }
   };
 
-#pragma unroll
-  for (int i = 0; i < kSlots - 1; ++i) {
-    issue(i, i);
-    cp_async_commit();
+  const int nring = a.nslots;
+  if (tid == 0) {
+    for (int q = 0; q < nring; ++q) {
+      mbar_init(smem_addr(&fullb[q]), 1);
+      mbar_init(smem_addr(&emptyb[q]), kWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int i = 0;; ++i) {
-    int d, r;
-    bool isA;
-    if (!unit_of(i, d, r, isA)) break;
-    issue(i + kSlots - 1, (i + kSlots - 1) % kSlots);
-    cp_async_commit();
-    cp_async_wait<kSlots - 1>();
-    __syncthreads();
-    const uint8_t* slot = ring + (size_t)(i % kSlots) * a.slot_bytes;
+  __syncthreads();
+  if (warp == kWarps) {  // ---------------- producer warp: keeps the ring full
+    uint32_t hostmask = 0;
+    for (int i = 0; i < nU; ++i) {
+      const int sl = i % nring, use = i / nring;
+      if (use > 0) mbar_wait(smem_addr(&emptyb[sl]), (uint32_t)(use - 1) & 1u, a.err);
+      issue(i, sl, hostmask);
+    }
+    cp_async_wait<0>();
+    return;
+  }
+  // ---------------- consumer warps
+  const int c0 = 2 * tig, c1 = 2 * tig + 1;  // C columns (token slots) of this lane
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};       // A task partials (kept across its units) / B unit sums
+  int hd = -1;                               // expert whose h is staged in hs
+  int rp = 0;                                // which half of red the next reduction uses
+  for (int i = 0; i < nU; ++i) {
+    int d, r, pa;
+    unit_of(i, d, r, pa);
+    const int sl = i % nring;
+    const int Te = R.wl_cnt[d], poff = R.wl_off[d];
+    if (pa < 0 && d != hd) {  // B unit of a new expert: stage its h (waiting, bounded, for its
+                              // A tasks) and the zero-point group sums
+      const int np2 = KP / 2, ip2 = I / 2;
+      const unsigned long long* hsrc = a.hbuf + (int64_t)d * a.tstride * np2;
+      for (int i0 = tid; i0 < Te * np2; i0 += 4 * kWarps * 32) {
+        unsigned long long v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // four reads in flight
+          const int ii = i0 + q * kWarps * 32;
+          v[q] = (ii < Te * np2 && ii % np2 < ip2) ? ld_relaxed_u64(hsrc + ii) : 0ull;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ii = i0 + q * kWarps * 32;
+          if (ii < Te * np2) {
+            const int n = ii / np2, c = ii % np2;
+            const uint32_t pr = c < ip2 ? payload_of(hsrc + ii, v[q], epoch, a.err) : 0u;
+            *reinterpret_cast<uint32_t*>(hs + (size_t)n * hstride + 2 * c) = pr;
+          }
+        }
+      }
+      const int tpg = G / kTileRows;  // 16-row sums per scale group
+      const unsigned long long* ssrc = a.hsum + (int64_t)d * a.tstride * (KP / 16);
+      for (int q = tid; q < ngI * Te; q += kWarps * 32) {
+        const int grp = q % ngI, n = q / ngI;
+        float sv = 0.f;
+        for (int j = 0; j < tpg; ++j) {
+          const int mt = grp * tpg + j;
+          if (mt < tilesI) {
+            const unsigned long long* pw = ssrc + n * (KP / 16) + mt;
+            sv += __uint_as_float(payload_of(pw, ld_relaxed_u64(pw), epoch, a.err));
+          }
+        }
+        csb[grp * 9 + n] = a.zcorr * sv;
+      }
+      hd = d;
+      consumer_sync();
+    }
 
-    if (isA) {
-      // ------------------------------------------------ A unit
-      const int mm = r & 1, mt = r >> 1;
-      const int Te = R.wl_cnt[d], poff = R.wl_off[d];
-      const int c0 = 2 * tig, c1 = 2 * tig + 1;  // C columns (token slots) of this lane
-      const int tg = g < Te ? R.perm[poff + g] / k : T;  // B column g: its token, or the zero row
-      const int z0i = c0 < Te ? R.perm[poff + c0] / k : 8;
-      const int z1i = c1 < Te ? R.perm[poff + c1] / k : 8;
-      for (int i = tid; i < ngH * kTileRows; i += blockDim.x) sf[i] = scale_at(slot + a_codes, i, a.sdt);
-      __syncthreads();
-      const uint16_t* xb = xs + (size_t)tg * xstride + 2 * tig;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int kb = warp; kb < nkbH; kb += kWarps)
-        tile_block_g<B, false>(G, slot + (size_t)kb * B * 512, lane, xb + kb * kBlockK, nullptr,
-                               sf + kb * gpb * kTileRows + g, csa + kb * gpb * 9 + z0i,
-                               csa + kb * gpb * 9 + z1i, acc);
-      float* rw = red + warp * 128;  // [row 16][col 8]
-      rw[g * 8 + c0] = acc[0];
-      rw[g * 8 + c1] = acc[1];
-      rw[(g + 8) * 8 + c0] = acc[2];
-      rw[(g + 8) * 8 + c1] = acc[3];
-      __syncthreads();
-      if (tid < 128) {
-        const int row = tid >> 3, col = tid & 7;
-        if (col < Te) {
-          float v = 0.f;
-#pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) v += red[ww * 128 + tid];
-          a.gu[(((int64_t)d * 2 + mm) * a.tstride + col) * I + mt * kTileRows + row] = v;
-        }
-      }
-      __syncthreads();
-      if (tid == 0) {  // release: the barrier above orders the CTA's stores before this fence
-        __threadfence();
-        atomicAdd(&a.done_a[d], 1u);
-      }
+    // ---- the unit's dot products: one code path for both kinds
+    // A (task d, tile r, part pa): warp w takes matrix w&1 (gate / up) and
+    //   the part's column blocks w>>1, w>>1 + 8, ...; B column g = token of
+    //   the expert's slot g, against the layer input.
+    // B (expert d, row block r): warp w takes row tile w&3 and column blocks
+    //   w>>2, w>>2 + 4, ...; B column g = the expert's slot g, against h.
+    // Columns g >= Te read a real row; their C columns are never used.
+    const uint8_t* slot = ring + (size_t)sl * a.slot_bytes;
+    const uint8_t* tbase;  // codes of the warp's tile, column block 0 of the unit
+    const uint8_t* scb;    // scales of the unit
+    const uint16_t* bbase;  // the lane's B-operand row at column block 0
+    const float* zb;        // zero-point sums at column block 0
+    int si, j0, jstep, jn, kbase;
+    if (pa >= 0) {
+      const int mm = warp & 1;
+      const int kb0 = pa * kbpp, nkp = min(nkbH, kb0 + kbpp) - kb0;
+      tbase = slot + (size_t)mm * nkp * B * 512;
+      scb = slot + (size_t)2 * nkp * B * 512 + (size_t)mm * nkp * gpb * kTileRows * ssz;
+      si = g;
+      j0 = warp >> 1, jstep = kWarps / 2, jn = nkp, kbase = kb0;
+      bbase = xs + (size_t)R.ptok[poff + (g < Te ? g : 0)] * xstride + 2 * tig;
+      zb = csa;
+      if (pa == 0) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     } else {
-      // ------------------------------------------------ B unit
-      const int rb = r;
-      const int Te = R.wl_cnt[d], poff = R.wl_off[d];
-      if (tid == 0) R.flag = wait_count(&a.done_a[d], (unsigned)nA, a.err) ? 1 : 0;
-      __syncthreads();
-      if (R.flag) {
-        // h = silu(g) * u for the expert's tokens, split into bf16 hi + lo
-        for (int j = 0; j < Te; ++j) {
-          const float* gj = a.gu + (((int64_t)d * 2 + 0) * a.tstride + j) * I;
-          const float* uj = a.gu + (((int64_t)d * 2 + 1) * a.tstride + j) * I;
-          for (int k0 = 0; k0 < KP; k0 += 4 * kWarps * 32) {
-            float gv[4], uv[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {  // all loads of the batch in flight at once
-              const int kk = k0 + q * kWarps * 32 + tid;
-              gv[q] = kk < I ? __ldcg(gj + kk) : 0.f;
-              uv[q] = kk < I ? __ldcg(uj + kk) : 0.f;
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int kk = k0 + q * kWarps * 32 + tid;
-              if (kk < KP) {
-                const float h = gv[q] / (1.0f + expf(-gv[q])) * uv[q];
-                const __nv_bfloat16 vh = __float2bfloat16_rn(h);
-                const __nv_bfloat16 vl = __float2bfloat16_rn(h - __bfloat162float(vh));
-                hh[j * hstride + kk] = __bfloat16_as_ushort(vh);
-                hl[j * hstride + kk] = __bfloat16_as_ushort(vl);
-              }
-            }
-          }
-        }
-        __syncthreads();
-        // scale-group sums of hi + lo, one warp per (group, token)
-        for (int q = warp; q < ngI * Te; q += kWarps) {
-          const int grp = q % ngI, j = q / ngI;
-          float sv = 0.f;
-          for (int i = lane; i < G; i += 32) {
-            const int kk = grp * G + i;
-            sv += bf16f(hh[j * hstride + kk]) + bf16f(hl[j * hstride + kk]);
-          }
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
-          if (lane == 0) csb[grp * 9 + j] = a.zcorr * sv;
-        }
-        for (int i = tid; i < (kBRows / kTileRows) * ngI * kTileRows; i += blockDim.x)
-          sf[i] = scale_at(slot + b_codes, i, a.sdt);
-        __syncthreads();
-        const int tl = warp & 3, kpar = warp >> 2;  // row tile within the block, column-block parity
-        const int c0 = 2 * tig, c1 = 2 * tig + 1;
-        const int hr = g < Te ? g : T;  // B column g: the expert's token slot g, or the zero row
-        const uint16_t* hb = hh + (size_t)hr * hstride + 2 * tig;
-        const uint16_t* lb = hl + (size_t)hr * hstride + 2 * tig;
-        const int z0i = c0 < Te ? c0 : 8, z1i = c1 < Te ? c1 : 8;
-        const uint8_t* tile = slot + (size_t)tl * nkbI * B * 512;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int tl = warp & 3;
+      tbase = slot + (size_t)tl * nkbI * B * 512;
+      scb = slot + b_codes;
+      si = tl * ngI * kTileRows + g;
+      j0 = warp >> 2, jstep = kWarps / 4, jn = nkbI, kbase = 0;
+      bbase = hs + (size_t)(g < Te ? g : 0) * hstride + 2 * tig;
+      zb = csb;
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    }
+    const int z0i = c0 < Te ? (pa >= 0 ? R.ptok[poff + c0] : c0) : 8;
+    const int z1i = c1 < Te ? (pa >= 0 ? R.ptok[poff + c1] : c1) : 8;
+    mbar_wait(smem_addr(&fullb[sl]), (uint32_t)(i / nring) & 1u, a.err);  // the unit's bytes are in
 #pragma unroll 1
-        for (int kb = kpar; kb < nkbI; kb += 2)
-          tile_block_g<B, true>(G, tile + (size_t)kb * B * 512, lane, hb + kb * kBlockK,
-                                lb + kb * kBlockK, sf + (tl * ngI + kb * gpb) * kTileRows + g,
-                                csb + kb * gpb * 9 + z0i, csb + kb * gpb * 9 + z1i, acc);
-        float* rw = red + warp * 128;
+    for (int j = j0; j < jn; j += jstep)
+      tile_block_g<B>(G, tbase + (size_t)j * B * 512, lane, bbase + (kbase + j) * kBlockK, scb,
+                      si + j * gpb * kTileRows, sdt, zb + (kbase + j) * gpb * 9 + z0i,
+                      zb + (kbase + j) * gpb * 9 + z1i, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&emptyb[sl]));  // this warp reads the slot no more
+
+    if (pa >= 0) {
+      if (pa == NP - 1) {  // A task complete: h for these 16 rows, published
+        const int mt = r;
+        float* rb2 = red + (rp & 1) * kWarps * 128;
+        ++rp;
+        float* rw = rb2 + warp * 128;  // [row 16][col 8]
         rw[g * 8 + c0] = acc[0];
         rw[g * 8 + c1] = acc[1];
         rw[(g + 8) * 8 + c0] = acc[2];
         rw[(g + 8) * 8 + c1] = acc[3];
-        __syncthreads();
-        for (int i = tid; i < kBRows * 8; i += blockDim.x) {
-          const int row = i >> 3, col = i & 7;
-          if (col < Te) {
-            const int t4 = row >> 4, r16 = row & 15;
-            const float o = red[t4 * 128 + r16 * 8 + col] + red[(t4 + 4) * 128 + r16 * 8 + col];
-            const int s = R.perm[poff + col];
-            a.obuf[(int64_t)s * H + rb * kBRows + row] = R.w[s] * o;
-          }
-        }
-        __syncthreads();
-        if (tid == 0) {  // release our rows, acquire everyone else's if we are last
-          __threadfence();
-          R.flag = (atomicAdd(&a.done_b[rb], 1u) == (unsigned)D - 1) ? 2 : 0;
-          __threadfence();
-        }
-        __syncthreads();
-        if (R.flag == 2) {  // every expert's contribution to these rows is in: combine
-          for (int i = tid; i < T * kBRows; i += blockDim.x) {
-            const int t = i / kBRows, row = rb * kBRows + i % kBRows;
-            float ov[kMaxTopK];
+        consumer_sync();
+        if (tid < 256) {
+          const int m2 = tid >> 7, e = tid & 127;
+          float v = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j)  // all k loads in flight, then summed in j order
-              if (j < k) ov[j] = __ldcg(a.obuf + (int64_t)(t * k + j) * H + row);
-            float o = 0.f;
+          for (int ww = 0; ww < kWarps / 2; ++ww) v += rb2[(2 * ww + m2) * 128 + e];
+          gus[tid] = v;
+        }
+        consumer_sync();
+        if (tid < 128) {
+          const int row = tid >> 3, col = tid & 7;
+          const float gv = gus[tid], uv = gus[128 + tid];
+          const float h = gv / (1.0f + expf(-gv)) * uv;
+          hq[col * 16 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+        }
+        consumer_sync();
+        if (tid < 8 * Te) {  // bf16 pairs (rows 2q, 2q+1) of token slot n
+          const int n = tid >> 3, q = tid & 7;
+          const uint32_t pr = (uint32_t)hq[n * 16 + 2 * q] | ((uint32_t)hq[n * 16 + 2 * q + 1] << 16);
+          st_relaxed_u64(a.hbuf + ((int64_t)d * a.tstride + n) * (KP / 2) + mt * 8 + q, tagged(pr, epoch));
+        } else if (tid >= 256 && tid < 256 + Te) {  // sum of the 16 bf16 values, rows ascending
+          const int n = tid - 256;
+          float sv = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j)
-              if (j < k) o += ov[j];
-            a.y[(int64_t)t * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-          }
+          for (int q = 0; q < 16; ++q) sv += bf16f(hq[n * 16 + q]);
+          st_relaxed_u64(a.hsum + ((int64_t)d * a.tstride + n) * (KP / 16) + mt,
+                         tagged(__float_as_uint(sv), epoch));
+        }
+      }
+    } else {
+      const int rb = r;
+      float* rb2 = red + (rp & 1) * kWarps * 128;
+      ++rp;
+      float* rw = rb2 + warp * 128;
+      rw[g * 8 + c0] = acc[0];
+      rw[g * 8 + c1] = acc[1];
+      rw[(g + 8) * 8 + c0] = acc[2];
+      rw[(g + 8) * 8 + c1] = acc[3];
+      consumer_sync();
+      for (int i2 = tid; i2 < kBRows * 8; i2 += kWarps * 32) {
+        const int row = i2 >> 3, col = i2 & 7;
+        if (col < Te) {
+          const int t4 = row >> 4, r16 = row & 15;
+          float o = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < kWarps / 4; ++ww) o += rb2[(4 * ww + t4) * 128 + r16 * 8 + col];
+          const int sl2 = R.perm[poff + col];
+          st_relaxed_u64(a.obuf + (int64_t)sl2 * H + rb * kBRows + row,
+                         tagged(__float_as_uint(R.w[sl2] * o), epoch));
         }
       }
     }
-    __syncthreads();  // the slot is refilled by the next iteration's issue
   }
-  cp_async_wait<0>();
+  // ---- combine: after all of its B units, a CTA of the last list sums every
+  // token's k slots (j ascending) of row blocks cidx, cidx + cs, ... into y.
+  // It waits (bounded) only on B units, which never wait on a combine.
+  if (Ch == 0 || !hostcta) {
+    for (int rb = cidx; rb < nB; rb += cs) {
+      for (int i2 = tid; i2 < T * kBRows; i2 += kWarps * 32) {
+        const int t = i2 / kBRows, row = rb * kBRows + i2 % kBRows;
+        unsigned long long v[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)  // all k reads in flight, then summed in j order
+          if (j < k) v[j] = ld_relaxed_u64(a.obuf + (int64_t)(t * k + j) * H + row);
+        float o = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (j < k)
+            o += __uint_as_float(payload_of(a.obuf + (int64_t)(t * k + j) * H + row, v[j], epoch, a.err));
+        a.y[(int64_t)t * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      }
+    }
+  }
 }
 
 template <int B>
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.blockDim = dim3((kWarps + 1) * 32);  // consumer warps + the producer warp
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -908,24 +1057,29 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   r.xsum = p.xsum;
   r.group = G;
   r.zcorr = zcorr;
-  r.done_a = p.done_a;
-  r.nda = p.max_distinct;
-  r.done_b = p.done_b;
-  r.ndb = H / kBRows;
+  r.epoch = &p.ctl->epoch;
   const int rgrid = (E + kRouterWarps - 1) / kRouterWarps;
   Plan::DecodeCfg& cf = p.dcfg[T];
   cudaError_t e = cudaSuccess;
   if (!cf.ready) {  // launch configuration for this batch size, once per plan
     const int KP = p.lay.m[2].kpad, ssz = scale_size(d.scale_dtype), b = d.weight_bits;
-    const size_t a_unit = (size_t)kTileRows * H * b / 8 + (size_t)(H / G) * kTileRows * ssz;
+    const int nkbH = H / kBlockK, NP = (nkbH + 7) / 8, kbpp = (nkbH + NP - 1) / NP;
+    const size_t a_unit = (size_t)2 * kbpp * b * 512 + (size_t)2 * kbpp * (kBlockK / G) * kTileRows * ssz;
     const size_t b_unit =
         (size_t)kBRows * KP * b / 8 + (size_t)(kBRows / kTileRows) * (KP / G) * kTileRows * ssz;
     cf.slot_bytes = (int)((std::max(a_unit, b_unit) + 127) / 128 * 128);
     const size_t ngH = H / G, ngI = KP / G;
-    cf.smem = ((size_t)(T + 1) * (H + 8) * 2 + 15) / 16 * 16 + (ngH * 9 * 4 + 15) / 16 * 16 +
-              (size_t)kSlots * cf.slot_bytes + ((size_t)2 * (T + 1) * (KP + 8) * 2 + 15) / 16 * 16 +
-              (ngI * 9 * 4 + 15) / 16 * 16 + (size_t)kWarps * 128 * 4 +
-              std::max(ngH, (size_t)(kBRows / kTileRows) * ngI) * kTileRows * 4;
+    const size_t fixed = ((size_t)T * (H + 8) * 2 + 15) / 16 * 16 + (ngH * 9 * 4 + 15) / 16 * 16 +
+                         ((size_t)T * (KP + 8) * 2 + 15) / 16 * 16 + (ngI * 9 * 4 + 15) / 16 * 16 +
+                         (size_t)2 * kWarps * 128 * 4 + 2 * 128 * 4 + 128 * 2;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device);
+    if (e != cudaSuccess) return e;
+    // ring depth: as many units as fit beside the static routing state (<= 8 KB)
+    const long avail = (long)optin - 8192 - (long)fixed;
+    cf.nslots = (int)std::min<long>(kMaxRing, avail / cf.slot_bytes);
+    if (cf.nslots < 2) return cudaErrorInvalidConfiguration;
+    cf.smem = fixed + (size_t)cf.nslots * cf.slot_bytes;
     cf.rsmem = (size_t)T * H * 2;
     const void* kfn = b == 2   ? (const void*)expert_decode_kernel<2>
                       : b == 3 ? (const void*)expert_decode_kernel<3>
@@ -942,7 +1096,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
       p.rsmem_set = cf.rsmem;
     }
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kWarps * 32, cf.smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, (kWarps + 1) * 32, cf.smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     // every CTA must be resident at once (B units wait on A units of other CTAs)
@@ -984,9 +1138,9 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.miss_list = p.miss_list;
   a.miss_count = p.miss_count;
   a.miss_cap = d.num_layers * p.max_distinct;
-  a.done_a = p.done_a;
-  a.done_b = p.done_b;
-  a.gu = p.hbuf;
+  a.epoch = &p.ctl->epoch;
+  a.hbuf = p.hbuf;
+  a.hsum = p.hsum;
   a.tstride = std::min(d.max_tokens, kDecodeMaxTokens);
   a.obuf = p.obuf;
   a.y = y;
@@ -999,6 +1153,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.zcorr = zcorr;
   a.err = p.err_dev;
   a.slot_bytes = cf.slot_bytes;
+  a.nslots = cf.nslots;
   const int b = d.weight_bits, grid = cf.grid;
   const size_t smem = cf.smem;
   switch (b) {

@@ -34,7 +34,7 @@ constexpr int kBlockK = 256;
 constexpr int kBRows = 64;           // rows of the down projection per B work unit
 constexpr int kDecodeMaxTokens = 8;  // forwards with T <= this use the decode path
 constexpr int kMaxTopK = 8;
-constexpr int kWarps = 8;            // warps per CTA of the decode expert kernel
+constexpr int kWarps = 16;           // warps per CTA of the decode expert kernel
 
 struct MatLayout {
   int rows, cols, kpad;  // cols = K; kpad = K rounded up to kBlockK
@@ -61,13 +61,10 @@ enum {
 // Error bits latched by kernels into the plan's error word.
 enum : uint32_t { kErrTimeout = 1u, kErrBounds = 2u };
 
-// Control words of one forward (device).  Reset by the router's last CTA.
+// Control words of the decode path (device).
 struct Ctl {
-  unsigned ticket;     // router: CTAs finished
-  unsigned queue;      // expert kernel: next work unit
-  unsigned ndistinct;  // D: distinct routed experts
-  unsigned nhost;      // how many of them (the first ones) are read from host memory
-  unsigned pad[4];
+  unsigned epoch;  // forward counter: bumped by the router kernel, tags the hand-off words
+  unsigned pad[7];
 };
 
 struct Plan {
@@ -107,11 +104,12 @@ struct Plan {
   int32_t* wl_off = nullptr;          // [maxD] offset into perm
   int32_t* wl_cnt = nullptr;          // [maxD] tokens routed to it
   const uint8_t** wl_blob = nullptr;  // [maxD] where to read it
-  unsigned* done_a = nullptr;         // [maxD]
-  unsigned* done_b = nullptr;         // [H / kBRows]
   Ctl* ctl = nullptr;
-  float* hbuf = nullptr;        // [maxD][2][decode T][I] gate and up projections
-  float* obuf = nullptr;        // [decode T * k][H] weighted expert outputs per slot
+  // Hand-off words between CTAs of the decode expert kernel: 32-bit payload in
+  // the low half, the forward's epoch in the high half (zeroed at creation).
+  unsigned long long* hbuf = nullptr;  // [maxD][decode T][kpad(I)/2] bf16 pairs of h
+  unsigned long long* hsum = nullptr;  // [maxD][decode T][kpad(I)/16] fp32 sums of 16 h values
+  unsigned long long* obuf = nullptr;  // [decode T * k][H] fp32 weighted expert outputs per slot
   float* xsum = nullptr;        // [decode T][H / G] scale-group sums of the layer input
   uint16_t* x_stage = nullptr;  // [maxT][H] for the host-buffer forward
   uint16_t* y_stage = nullptr;
@@ -142,7 +140,7 @@ struct Plan {
   struct DecodeCfg {
     bool ready = false;
     size_t smem = 0, rsmem = 0;
-    int grid = 0, slot_bytes = 0;
+    int grid = 0, slot_bytes = 0, nslots = 0;
   } dcfg[kDecodeMaxTokens + 1];
   size_t dsmem_set = 0, rsmem_set = 0;  // largest max-dynamic-smem attributes set so far
 

@@ -336,7 +336,7 @@ void release(Plan* p) {
   for (auto* b : p->bias) cudaFree(b);
   void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
-                 p->wl_blob, p->done_a, p->done_b, p->ctl, p->hbuf, p->obuf, p->xsum, p->x_stage,
+                 p->wl_blob, p->ctl, p->hbuf, p->hsum, p->obuf, p->xsum, p->x_stage,
                  p->y_stage, p->slot_of, p->slot_owner, p->lfu_count, p->lfu_last, p->miss_list,
                  p->miss_count, p->adm_list, p->adm_count, p->stats};
   for (void* v : dev)
@@ -390,7 +390,7 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
 
   // HBM need: arena + routers + tables + scratch, against free memory minus headroom
   const int64_t scratch = maxT * E * 4 + maxT * k * 16 + (E + 1) * 8 + maxD * 32 +
-                          2 * maxD * decT * I * 4 + decT * k * H * 4 + 2 * maxT * H * 2 + 4096;
+                          maxD * decT * (I + 256) * 5 + decT * k * H * 8 + 2 * maxT * H * 2 + 4096;
   const int64_t lfu = d.cache_policy == MOE_POLICY_LFU
                           ? LE * 12 + slots * 8 + (int64_t)d.num_layers * maxD * 8
                           : 0;
@@ -460,10 +460,10 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   ALLOC(p->wl_off, maxD);
   ALLOC(p->wl_cnt, maxD);
   ALLOC(p->wl_blob, maxD);
-  ALLOC(p->done_a, maxD);
-  ALLOC(p->done_b, H / kBRows);
   ALLOC(p->ctl, 1);
-  ALLOC(p->hbuf, 2 * maxD * decT * I);
+  const int64_t KPI = p->lay.m[2].kpad;
+  ALLOC(p->hbuf, maxD * decT * (KPI / 2));
+  ALLOC(p->hsum, maxD * decT * (KPI / 16));
   ALLOC(p->obuf, decT * k * H);
   ALLOC(p->xsum, decT * (H / d.group_size));
   ALLOC(p->x_stage, maxT * H);
@@ -494,6 +494,9 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   cudaMemset(p->blob_hbm, 0, LE * sizeof(void*));
   cudaMemset(p->blob_host, 0, LE * sizeof(void*));
   cudaMemset(p->ctl, 0, sizeof(Ctl));
+  cudaMemset(p->hbuf, 0, (size_t)maxD * decT * (KPI / 2) * 8);  // epoch 0: never current
+  cudaMemset(p->hsum, 0, (size_t)maxD * decT * (KPI / 16) * 8);
+  cudaMemset(p->obuf, 0, (size_t)decT * k * H * 8);
   cudaMemset(p->stats, 0, (size_t)d.num_layers * kNumStats * 8);
   if (d.cache_policy == MOE_POLICY_LFU) {
     cudaMemset(p->slot_of, 0xff, LE * 4);
