@@ -84,13 +84,18 @@ struct RouterArgs {
 // Logits in the fixed order: lane j accumulates, from +0, fmaf(x[i], w[i], acc)
 // over i = 256m + 8j + r (m ascending, r ascending); the 32 lane sums are then
 // combined by xor-butterfly adds with offsets 16, 8, 4, 2, 1 (every lane ends
-// with the same value); the bias is added last.
+// with the same value); the bias is added last.  Grid: (experts / 4) x
+// (token pairs); one warp per (expert, pair of tokens), the pair's inputs
+// converted to fp32 in shared memory once per CTA.
+constexpr int kRouterTok = 2;
+
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_logits_kernel(RouterArgs a) {
   extern __shared__ uint4 r_smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(r_smem);  // [T][H] bf16
+  float* xf = reinterpret_cast<float*>(r_smem);  // [kRouterTok][H] fp32
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T = a.T, H = a.H, E = a.E;
+  const int H = a.H, E = a.E;
+  const int t0 = blockIdx.y * kRouterTok, nt = min(kRouterTok, a.T - t0);
   // the dependent expert kernel may be scheduled now: it waits for this
   // grid's completion itself (griddepcontrol.wait) and this grid never waits on it
   asm volatile("griddepcontrol.launch_dependents;");
@@ -103,34 +108,39 @@ router_logits_kernel(RouterArgs a) {
 #pragma unroll
   for (int q = 0; q < 16; ++q)
     if (ev && q < nm) wv[q] = __ldg(w + q * 32 + lane);
-  {  // x -> shared memory, eight 16-byte loads in flight per thread
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    uint4* dst = reinterpret_cast<uint4*>(xs);
-    const int n = T * H / 8;
-    for (int i0 = 0; i0 < n; i0 += 8 * kRouterWarps * 32) {
-      uint4 v[8];
+  {  // this pair's inputs -> fp32 shared memory, four 16-byte loads in flight per thread
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)t0 * H);
+    const int n = nt * H / 8;
+    for (int i0 = 0; i0 < n; i0 += 4 * kRouterWarps * 32) {
+      uint4 v[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const int i = i0 + q * kRouterWarps * 32 + tid;
         if (i < n) v[q] = __ldg(src + i);
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const int i = i0 + q * kRouterWarps * 32 + tid;
-        if (i < n) dst[i] = v[q];
+        if (i < n) {
+          float4* d = reinterpret_cast<float4*>(xf + (size_t)i * 8);
+          d[0] = make_float4(bf16f(v[q].x & 0xffffu), bf16f(v[q].x >> 16), bf16f(v[q].y & 0xffffu),
+                             bf16f(v[q].y >> 16));
+          d[1] = make_float4(bf16f(v[q].z & 0xffffu), bf16f(v[q].z >> 16), bf16f(v[q].w & 0xffffu),
+                             bf16f(v[q].w >> 16));
+        }
       }
     }
   }
-  if (blockIdx.x == 0 && tid == 0) {  // a new epoch for this forward's hand-off words (never 0)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {  // a new epoch for this forward (never 0)
     const unsigned ep = *a.epoch + 1u;
     *a.epoch = ep ? ep : 1u;
   }
   __syncthreads();
 
   if (ev) {
-    float acc[kDecodeMaxTokens];
+    float acc[kRouterTok];
 #pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.0f;
     for (int m0 = 0; m0 < nm; m0 += 16) {
       if (m0 > 0) {
 #pragma unroll
@@ -141,39 +151,40 @@ router_logits_kernel(RouterArgs a) {
       for (int q = 0; q < 16; ++q) {
         if (m0 + q >= nm) break;
         const uint32_t wq[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+        float wf[8];
 #pragma unroll
-        for (int t = 0; t < kDecodeMaxTokens; ++t) {
-          if (t >= T) break;
-          const uint4 xv = reinterpret_cast<const uint4*>(xs + t * H)[(m0 + q) * 32 + lane];
-          const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+        for (int r = 0; r < 8; ++r) wf[r] = (r & 1) ? __uint_as_float(wq[r >> 1] & 0xffff0000u)
+                                                    : bf16f(wq[r >> 1] & 0xffffu);
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const uint32_t xb = (r & 1) ? (xq[r >> 1] >> 16) : (xq[r >> 1] & 0xffffu);
-            const uint32_t wb = (r & 1) ? (wq[r >> 1] >> 16) : (wq[r >> 1] & 0xffffu);
-            acc[t] = fmaf(bf16f(xb), bf16f(wb), acc[t]);
-          }
+        for (int t = 0; t < kRouterTok; ++t) {
+          if (t >= nt) break;
+          const float4* xv = reinterpret_cast<const float4*>(xf + (size_t)t * H + ((m0 + q) * 32 + lane) * 8);
+          const float4 xa = xv[0], xb = xv[1];
+          const float xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+          for (int r = 0; r < 8; ++r) acc[t] = fmaf(xr[r], wf[r], acc[t]);
         }
       }
     }
     const float b = a.bias[e];
 #pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t) {
-      if (t >= T) break;
+    for (int t = 0; t < kRouterTok; ++t) {
+      if (t >= nt) break;
       float v = acc[t];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) a.logits[t * E + e] = v + b;
+      if (lane == 0) a.logits[(t0 + t) * E + e] = v + b;
     }
   }
-  // scale-group sums of x: pair q = (t, group), one warp each
+  // scale-group sums of x: pair q = (t, group) of this CTA's tokens, one warp each
   const int ng = H / a.group;
-  for (int q = blockIdx.x * kRouterWarps + warp; q < T * ng; q += gridDim.x * kRouterWarps) {
+  for (int q = blockIdx.x * kRouterWarps + warp; q < nt * ng; q += gridDim.x * kRouterWarps) {
     const int t = q / ng, grp = q % ng;
     float v = 0.f;
-    for (int i = lane; i < a.group; i += 32) v += bf16f(xs[t * H + grp * a.group + i]);
+    for (int i = lane; i < a.group; i += 32) v += xf[(size_t)t * H + grp * a.group + i];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) a.xsum[q] = a.zcorr * v;
+    if (lane == 0) a.xsum[(t0 + t) * ng + grp] = a.zcorr * v;
   }
 }
 
@@ -359,14 +370,37 @@ __device__ __forceinline__ uint32_t pair_of(const uint32_t (&w)[4 * B], int P) {
   }
 }
 
+// B-operand rows in shared memory are kept in fragment order: for column
+// block kb (256 columns), quad tig (lane % 4) and 16-column step kt, the two
+// bf16 pairs a lane feeds one mma.m16n8k16 (columns kt*16 + 2tig, +1 and
+// kt*16 + 8 + 2tig, +9) sit at byte kb*576 + tig*144 + kt*8 (+4), so one
+// 16-byte load serves two steps.  The 144-byte quad stride and a row stride
+// of 64 (mod 128) bytes keep a quarter-warp's loads on distinct banks.
+__host__ __device__ inline int frag_row_bytes(int nkb) { return nkb * 576 + ((nkb & 1) ? 0 : 64); }
+__device__ __forceinline__ int frag_offset(int col) {  // byte offset of the pair holding column col (even)
+  const int kb = col >> 8, kk = col & 255;
+  return kb * 576 + ((kk & 7) >> 1) * 144 + (kk >> 4) * 8 + ((kk >> 3) & 1) * 4;
+}
+
+__device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // One 256-column block of a 16-row weight tile (codes at `tile`, the lane's
-// words at tile + q*512 + lane*16) against the lane's B-operand row `bh`: for
-// every scale group gi of the block, acc += s * (C_gi - z), where s is the
-// scale of the lane's row g (element si + gi*16 of `scb`) or row g + 8
-// (si + gi*16 + 8), and z = z0[gi*9] / z1[gi*9] for the lane's two C columns.
-// Two accumulator chains (even / odd steps) keep MMAs in flight.
+// words at tile + q*512 + lane*16) against the lane's B-operand fragments
+// `bf` (its quad's 144 bytes of the block): for every scale group gi of the
+// block, acc += s * (C_gi - z), where s is the scale of the lane's row g
+// (element si + gi*16 of `scb`) or row g + 8 (si + gi*16 + 8), and
+// z = z0[gi*9] / z1[gi*9] for the lane's two C columns.  Two accumulator
+// chains (even / odd steps) keep MMAs in flight; each group's first MMA of a
+// chain starts from zero.
 template <int B, int G>
-__device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const uint16_t* bh,
+__device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const uint8_t* bf,
                                            const uint8_t* scb, int si, int sdt, const float* z0,
                                            const float* z1, float (&acc)[4]) {
   uint32_t w[4 * B];
@@ -378,37 +412,44 @@ __device__ __forceinline__ void tile_block(const uint8_t* tile, int lane, const 
     w[4 * q + 2] = v.z;
     w[4 * q + 3] = v.w;
   }
-  float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+  float e0[4], e1[4];
   constexpr int kSteps = G / 16;
 #pragma unroll
-  for (int kt = 0; kt < 16; ++kt) {
-    const uint32_t a0 = pair_of<B>(w, 4 * kt), a1 = pair_of<B>(w, 4 * kt + 1);
-    const uint32_t a2 = pair_of<B>(w, 4 * kt + 2), a3 = pair_of<B>(w, 4 * kt + 3);
-    const uint32_t h0 = *reinterpret_cast<const uint32_t*>(bh + kt * 16);
-    const uint32_t h1 = *reinterpret_cast<const uint32_t*>(bh + kt * 16 + 8);
-    mma_bf16((kt & 1) ? e1 : e0, a0, a1, a2, a3, h0, h1);
-    if ((kt + 1) % kSteps == 0) {  // end of scale group gi (folded at compile time)
-      const int gi = (kt + 1) / kSteps - 1;
-      const float s0 = scale_at(scb, si + gi * 16, sdt), s1 = scale_at(scb, si + gi * 16 + 8, sdt);
-      const float y0 = z0[gi * 9], y1 = z1[gi * 9];
-      acc[0] = fmaf(s0, (e0[0] + e1[0]) - y0, acc[0]);
-      acc[1] = fmaf(s0, (e0[1] + e1[1]) - y1, acc[1]);
-      acc[2] = fmaf(s1, (e0[2] + e1[2]) - y0, acc[2]);
-      acc[3] = fmaf(s1, (e0[3] + e1[3]) - y1, acc[3]);
+  for (int k2 = 0; k2 < 8; ++k2) {
+    const uint4 hv = *reinterpret_cast<const uint4*>(bf + k2 * 16);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) e0[q] = e1[q] = 0.f;
+    for (int h = 0; h < 2; ++h) {
+      const int kt = 2 * k2 + h;
+      const uint32_t a0 = pair_of<B>(w, 4 * kt), a1 = pair_of<B>(w, 4 * kt + 1);
+      const uint32_t a2 = pair_of<B>(w, 4 * kt + 2), a3 = pair_of<B>(w, 4 * kt + 3);
+      const uint32_t h0 = h ? hv.z : hv.x, h1 = h ? hv.w : hv.y;
+      if (kt % kSteps < 2) {
+        if (h) mma_bf16_zc(e1, a0, a1, a2, a3, h0, h1);
+        else mma_bf16_zc(e0, a0, a1, a2, a3, h0, h1);
+      } else {
+        mma_bf16(h ? e1 : e0, a0, a1, a2, a3, h0, h1);
+      }
+      if ((kt + 1) % kSteps == 0) {  // end of scale group gi (folded at compile time)
+        const int gi = (kt + 1) / kSteps - 1;
+        const float s0 = scale_at(scb, si + gi * 16, sdt), s1 = scale_at(scb, si + gi * 16 + 8, sdt);
+        const float y0 = z0[gi * 9], y1 = z1[gi * 9];
+        acc[0] = fmaf(s0, (e0[0] + e1[0]) - y0, acc[0]);
+        acc[1] = fmaf(s0, (e0[1] + e1[1]) - y1, acc[1]);
+        acc[2] = fmaf(s1, (e0[2] + e1[2]) - y0, acc[2]);
+        acc[3] = fmaf(s1, (e0[3] + e1[3]) - y1, acc[3]);
+      }
     }
   }
 }
 
 template <int B>
 __device__ __forceinline__ void tile_block_g(int G, const uint8_t* tile, int lane,
-                                             const uint16_t* bh, const uint8_t* scb, int si,
+                                             const uint8_t* bf, const uint8_t* scb, int si,
                                              int sdt, const float* z0, const float* z1,
                                              float (&acc)[4]) {
-  if (G == 128) tile_block<B, 128>(tile, lane, bh, scb, si, sdt, z0, z1, acc);
-  else if (G == 64) tile_block<B, 64>(tile, lane, bh, scb, si, sdt, z0, z1, acc);
-  else tile_block<B, 32>(tile, lane, bh, scb, si, sdt, z0, z1, acc);
+  if (G == 128) tile_block<B, 128>(tile, lane, bf, scb, si, sdt, z0, z1, acc);
+  else if (G == 64) tile_block<B, 64>(tile, lane, bf, scb, si, sdt, z0, z1, acc);
+  else tile_block<B, 32>(tile, lane, bf, scb, si, sdt, z0, z1, acc);
 }
 
 struct Routing {  // per-CTA copy of this forward's routing (shared memory)
@@ -417,14 +458,11 @@ struct Routing {  // per-CTA copy of this forward's routing (shared memory)
   int perm[kMaxSlots];                // slots ordered by (expert, token)
   int ptok[kMaxSlots];                // token of perm[p]
   int rank[kMaxSlots];                // position of slot s in perm
-  int first[kMaxSlots];               // perm position p starts a distinct expert: 1 = HBM, 2 = host
-  const uint8_t* pblob[kMaxSlots];
   int wl_off[kMaxSlots];              // distinct expert d (host-resident first): perm offset,
   int wl_cnt[kMaxSlots];              //   token count,
   int wl_e[kMaxSlots];                //   expert id,
   const uint8_t* wl_blob[kMaxSlots];  //   and where its weights are read from
   int D, nh;
-  int flag;
 };
 
 template <int B>
@@ -437,18 +475,18 @@ expert_decode_kernel(ExpertArgs a) {
   const int g = lane >> 2, tig = lane & 3;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, KP = a.kpadI, G = a.group;
   const int ngH = H / G, ngI = KP / G, nkbH = H / kBlockK, nkbI = KP / kBlockK;
-  const int xstride = H + 8, hstride = KP + 8;  // bf16 elements; pads spread rows over banks
+  const int xrow = frag_row_bytes(nkbH), hrow = frag_row_bytes(nkbI);  // fragment-ordered row bytes
   const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
   const int gpb = kBlockK / G;  // scale groups per 256-column block
   const int sdt = a.sdt;
 
   // shared memory carve-up (all offsets multiples of 16 bytes)
-  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);  // [T][H+8] layer input
-  size_t off = ((size_t)T * xstride * 2 + 15) / 16 * 16;
+  uint8_t* xs = sm;  // [T] fragment-ordered rows of the layer input
+  size_t off = (size_t)T * xrow;
   float* csa = reinterpret_cast<float*>(sm + off);  // [ngH][9], column 8 = 0
   off += ((size_t)ngH * 9 * 4 + 15) / 16 * 16;
-  uint16_t* hs = reinterpret_cast<uint16_t*>(sm + off);  // [T][KP+8] staged h of one expert
-  off += ((size_t)T * hstride * 2 + 15) / 16 * 16;
+  uint8_t* hs = sm + off;  // [T] fragment-ordered rows of one expert's h
+  off += (size_t)T * hrow;
   float* csb = reinterpret_cast<float*>(sm + off);  // [ngI][9], column 8 = 0
   off += ((size_t)ngI * 9 * 4 + 15) / 16 * 16;
   float* red = reinterpret_cast<float*>(sm + off);  // [2][kWarps][16][8] per-warp partials
@@ -474,7 +512,13 @@ expert_decode_kernel(ExpertArgs a) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int c = c0 + q * kWarps * 32 + tid;
-        if (c < H / 8) *reinterpret_cast<uint4*>(xs + t * xstride + c * 8) = v[q];
+        if (c < H / 8) {  // 8 columns = the same step and half for the four quads
+          uint32_t* dq = reinterpret_cast<uint32_t*>(xs + (size_t)t * xrow + frag_offset(c * 8));
+          dq[0] = v[q].x;
+          dq[36] = v[q].y;  // +144 bytes per quad
+          dq[72] = v[q].z;
+          dq[108] = v[q].w;
+        }
       }
     }
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -614,52 +658,69 @@ expert_decode_kernel(ExpertArgs a) {
   }
   __syncthreads();
 
-  // ---- grouping by (expert, token) and the distinct-expert work list
+  // ---- grouping by (expert, token) and the distinct-expert work list, by
+  // warp 0 alone (n = T*k <= 64: two slots / perm positions per lane)
   const int n = T * k;
-  for (int s = tid; s < n; s += blockDim.x) {
-    const int key = R.e[s] * T + s / k;
-    int r = 0;
-    for (int q = 0; q < n; ++q) r += (R.e[q] * T + q / k) < key;
-    R.rank[s] = r;
-    R.perm[r] = s;
-    R.ptok[r] = s / k;
-  }
-  __syncthreads();
-  for (int p = tid; p < n; p += blockDim.x) {
-    const int ee = R.e[R.perm[p]];
-    int f = 0;
-    if (p == 0 || R.e[R.perm[p - 1]] != ee) {
-      const uint8_t* hb = a.blob_hbm[ee];
-      f = hb ? 1 : 2;
-      R.pblob[p] = hb ? hb : a.blob_host[ee];
+  if (warp == 0) {
+    constexpr unsigned kAll = 0xffffffffu;
+    const int s0 = lane, s1 = lane + 32;
+    const int key0 = s0 < n ? R.e[s0] * T + s0 / k : 0x7fffffff;  // unique per slot
+    const int key1 = s1 < n ? R.e[s1] * T + s1 / k : 0x7fffffff;
+    int r0 = 0, r1 = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {  // rank = number of smaller keys
+      const int o0 = __shfl_sync(kAll, key0, j), o1 = __shfl_sync(kAll, key1, j);
+      r0 += (o0 < key0) + (o1 < key0);
+      r1 += (o0 < key1) + (o1 < key1);
     }
-    R.first[p] = f;
-  }
-  __syncthreads();
-  for (int p = tid; p < n; p += blockDim.x) {
-    const int f = R.first[p];
-    if (!f) continue;
-    int nh_all = 0, before = 0;
-    for (int q = 0; q < n; ++q) {
-      nh_all += R.first[q] == 2;
-      before += q < p && R.first[q] == f;
+    if (s0 < n) {
+      R.rank[s0] = r0;
+      R.perm[r0] = s0;
+      R.ptok[r0] = s0 / k;
     }
-    const int d = f == 2 ? before : nh_all + before;
-    int cnt = 1;
-    while (p + cnt < n && R.first[p + cnt] == 0) ++cnt;
-    R.wl_off[d] = p;
-    R.wl_cnt[d] = cnt;
-    R.wl_e[d] = R.e[R.perm[p]];
-    R.wl_blob[d] = R.pblob[p];
-  }
-  if (tid == 0) {
-    int nd = 0, nh = 0;
-    for (int q = 0; q < n; ++q) {
-      nd += R.first[q] != 0;
-      nh += R.first[q] == 2;
+    if (s1 < n) {
+      R.rank[s1] = r1;
+      R.perm[r1] = s1;
+      R.ptok[r1] = s1 / k;
     }
-    R.D = nd;
-    R.nh = nh;
+    __syncwarp();
+    // perm positions p0 = lane, p1 = lane + 32: expert, first-of-run flag, residence
+    const int pe0 = s0 < n ? R.e[R.perm[s0]] : -1, pe1 = s1 < n ? R.e[R.perm[s1]] : -1;
+    const int up0 = __shfl_up_sync(kAll, pe0, 1), up1 = __shfl_up_sync(kAll, pe1, 1);
+    const int last0 = __shfl_sync(kAll, pe0, 31);
+    const bool f0 = s0 < n && (lane == 0 || up0 != pe0);
+    const bool f1 = s1 < n && ((lane == 0 ? last0 : up1) != pe1);
+    const uint8_t* hb0 = f0 ? a.blob_hbm[pe0] : nullptr;  // both tables read at once
+    const uint8_t* hh0 = f0 ? a.blob_host[pe0] : nullptr;
+    const uint8_t* hb1 = f1 ? a.blob_hbm[pe1] : nullptr;
+    const uint8_t* hh1 = f1 ? a.blob_host[pe1] : nullptr;
+    const unsigned F0 = __ballot_sync(kAll, f0), F1 = __ballot_sync(kAll, f1);
+    const unsigned X0 = __ballot_sync(kAll, f0 && !hb0), X1 = __ballot_sync(kAll, f1 && !hb1);  // host
+    const int nh = __popc(X0) + __popc(X1), nd = __popc(F0) + __popc(F1);
+    const unsigned lt = (1u << lane) - 1u;
+    if (f0) {  // host-resident experts first, each group in perm order
+      const int d = !hb0 ? __popc(X0 & lt) : nh + __popc((F0 & ~X0) & lt);
+      const unsigned above = F0 & ~lt & ~(1u << lane);
+      const int nxt = above ? __ffs(above) - 1 : (F1 ? 32 + __ffs(F1) - 1 : n);
+      R.wl_off[d] = s0;
+      R.wl_cnt[d] = min(nxt, n) - s0;
+      R.wl_e[d] = pe0;
+      R.wl_blob[d] = hb0 ? hb0 : hh0;
+    }
+    if (f1) {
+      const int d = !hb1 ? __popc(X0) + __popc(X1 & lt)
+                         : nh + __popc(F0 & ~X0) + __popc((F1 & ~X1) & lt);
+      const unsigned above = F1 & ~lt & ~(1u << lane);
+      const int nxt = above ? 32 + __ffs(above) - 1 : n;
+      R.wl_off[d] = s1;
+      R.wl_cnt[d] = nxt - s1;
+      R.wl_e[d] = pe1;
+      R.wl_blob[d] = hb1 ? hb1 : hh1;
+    }
+    if (lane == 0) {
+      R.D = nd;
+      R.nh = nh;
+    }
   }
   __syncthreads();
   const int D = R.D;
@@ -871,7 +932,7 @@ expert_decode_kernel(ExpertArgs a) {
           if (ii < Te * np2) {
             const int n = ii / np2, c = ii % np2;
             const uint32_t pr = c < ip2 ? payload_of(hsrc + ii, v[q], epoch, a.err) : 0u;
-            *reinterpret_cast<uint32_t*>(hs + (size_t)n * hstride + 2 * c) = pr;
+            *reinterpret_cast<uint32_t*>(hs + (size_t)n * hrow + frag_offset(2 * c)) = pr;
           }
         }
       }
@@ -903,7 +964,7 @@ expert_decode_kernel(ExpertArgs a) {
     const uint8_t* slot = ring + (size_t)sl * a.slot_bytes;
     const uint8_t* tbase;  // codes of the warp's tile, column block 0 of the unit
     const uint8_t* scb;    // scales of the unit
-    const uint16_t* bbase;  // the lane's B-operand row at column block 0
+    const uint8_t* bbase;   // the lane's quad of its B-operand row, column block 0
     const float* zb;        // zero-point sums at column block 0
     int si, j0, jstep, jn, kbase;
     if (pa >= 0) {
@@ -913,7 +974,7 @@ expert_decode_kernel(ExpertArgs a) {
       scb = slot + (size_t)2 * nkp * B * 512 + (size_t)mm * nkp * gpb * kTileRows * ssz;
       si = g;
       j0 = warp >> 1, jstep = kWarps / 2, jn = nkp, kbase = kb0;
-      bbase = xs + (size_t)R.ptok[poff + (g < Te ? g : 0)] * xstride + 2 * tig;
+      bbase = xs + (size_t)R.ptok[poff + (g < Te ? g : 0)] * xrow + tig * 144;
       zb = csa;
       if (pa == 0) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     } else {
@@ -922,7 +983,7 @@ expert_decode_kernel(ExpertArgs a) {
       scb = slot + b_codes;
       si = tl * ngI * kTileRows + g;
       j0 = warp >> 2, jstep = kWarps / 4, jn = nkbI, kbase = 0;
-      bbase = hs + (size_t)(g < Te ? g : 0) * hstride + 2 * tig;
+      bbase = hs + (size_t)(g < Te ? g : 0) * hrow + tig * 144;
       zb = csb;
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
@@ -931,7 +992,7 @@ expert_decode_kernel(ExpertArgs a) {
     mbar_wait(smem_addr(&fullb[sl]), (uint32_t)(i / nring) & 1u, a.err);  // the unit's bytes are in
 #pragma unroll 1
     for (int j = j0; j < jn; j += jstep)
-      tile_block_g<B>(G, tbase + (size_t)j * B * 512, lane, bbase + (kbase + j) * kBlockK, scb,
+      tile_block_g<B>(G, tbase + (size_t)j * B * 512, lane, bbase + (kbase + j) * 576, scb,
                       si + j * gpb * kTileRows, sdt, zb + (kbase + j) * gpb * 9 + z0i,
                       zb + (kbase + j) * gpb * 9 + z1i, acc);
     __syncwarp();
@@ -1058,7 +1119,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   r.group = G;
   r.zcorr = zcorr;
   r.epoch = &p.ctl->epoch;
-  const int rgrid = (E + kRouterWarps - 1) / kRouterWarps;
+  const dim3 rgrid((E + kRouterWarps - 1) / kRouterWarps, (T + kRouterTok - 1) / kRouterTok);
   Plan::DecodeCfg& cf = p.dcfg[T];
   cudaError_t e = cudaSuccess;
   if (!cf.ready) {  // launch configuration for this batch size, once per plan
@@ -1069,8 +1130,8 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
         (size_t)kBRows * KP * b / 8 + (size_t)(kBRows / kTileRows) * (KP / G) * kTileRows * ssz;
     cf.slot_bytes = (int)((std::max(a_unit, b_unit) + 127) / 128 * 128);
     const size_t ngH = H / G, ngI = KP / G;
-    const size_t fixed = ((size_t)T * (H + 8) * 2 + 15) / 16 * 16 + (ngH * 9 * 4 + 15) / 16 * 16 +
-                         ((size_t)T * (KP + 8) * 2 + 15) / 16 * 16 + (ngI * 9 * 4 + 15) / 16 * 16 +
+    const size_t fixed = (size_t)T * frag_row_bytes(H / kBlockK) + (ngH * 9 * 4 + 15) / 16 * 16 +
+                         (size_t)T * frag_row_bytes(KP / kBlockK) + (ngI * 9 * 4 + 15) / 16 * 16 +
                          (size_t)2 * kWarps * 128 * 4 + 2 * 128 * 4 + 128 * 2;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device);
@@ -1080,7 +1141,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
     cf.nslots = (int)std::min<long>(kMaxRing, avail / cf.slot_bytes);
     if (cf.nslots < 2) return cudaErrorInvalidConfiguration;
     cf.smem = fixed + (size_t)cf.nslots * cf.slot_bytes;
-    cf.rsmem = (size_t)T * H * 2;
+    cf.rsmem = (size_t)kRouterTok * H * 4;
     const void* kfn = b == 2   ? (const void*)expert_decode_kernel<2>
                       : b == 3 ? (const void*)expert_decode_kernel<3>
                                : (const void*)expert_decode_kernel<4>;
