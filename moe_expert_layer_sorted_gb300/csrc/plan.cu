@@ -319,6 +319,11 @@ moe_status validate(const moe_plan_desc* d, std::string& why) {
     why = "cache_slots must be in [0, L*E]";
     return MOE_ERR_INVALID;
   }
+  if (d->cache_policy == MOE_POLICY_LFU &&
+      (int64_t)d->num_layers * std::min<int64_t>(d->num_experts, (int64_t)d->max_tokens * d->top_k) > 50000) {
+    why = "LFU cache: num_layers * min(E, max_tokens * top_k) must be <= 50000 (misses queued per step)";
+    return MOE_ERR_INVALID;
+  }
   if (d->host_overlap != 0 && d->host_overlap != 1) { why = "host_overlap must be 0 or 1"; return MOE_ERR_INVALID; }
   if (d->aging_period < 0) { why = "aging_period must be >= 0"; return MOE_ERR_INVALID; }
   return MOE_OK;

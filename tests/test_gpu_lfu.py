@@ -1,0 +1,113 @@
+"""LFU expert cache on the GPU against the oracle's cache simulator.
+
+A small cached-decode stack (the shape family of "Running a 24k-expert MoE on
+a single 32 GB card", sections 2-3: every expert pinned in host memory, an
+HBM cache admitted by access frequency, skewed popularity with drifting
+router bias) runs step by step through the C-ABI.  The distinct experts each
+forward routes to are read back and replayed through ``oracle.cache_sim``:
+per-(step, layer) hits and misses, admissions, evictions and the final slot
+owners must match exactly.  Layer outputs must be bit-identical to a plan
+that keeps every expert in HBM (placement changes no output bit)."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+WL = W.Workload("lfu-small", 3, 24, 256, 128, 2, (2,), 2, 64, W.SC_F16, "zipf", 1.2,
+                cache_frac=0.25, steps=24, drift=0.05)
+
+
+def _x(step, layer, T):
+    import torch
+    return torch.from_numpy(W.tokens(WL, step, layer, T).view(np.int16).copy()).cuda().view(torch.bfloat16)
+
+
+def test_lfu_matches_cache_simulator():
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    plan, info = harness.build_plan(WL)
+    ref, _ = harness.build_plan(WL, all_hbm=True)
+    C = plan.desc.cache_slots
+    assert C == int(np.floor(0.25 * 3 * 24))
+    L, E, k, T = WL.layers, WL.experts, WL.top_k, 2
+    maxd = T * k
+    access = np.full((WL.steps, L, maxd), -1, np.int32)
+    hits = np.zeros((WL.steps, L), np.int64)
+    misses = np.zeros((WL.steps, L), np.int64)
+    biases = [info["routers"][l][1].copy() for l in range(L)]
+    plan.stats(-1, reset=True)
+    for s in range(WL.steps):
+        for l in range(L):
+            x = _x(s, l, T)
+            y = torch.empty_like(x)
+            y_ref = torch.empty_like(x)
+            idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+            plan.forward(l, x, y, dbg=dict(topk_idx=idx))
+            ref.forward(l, x, y_ref)
+            torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (s, l)
+            d = np.unique(idx.cpu().numpy())
+            access[s, l, : len(d)] = d
+            st = plan.stats(l, reset=True)
+            hits[s, l], misses[s, l] = st["hits"], st["misses"]
+            assert st["accesses"] == len(d)
+        plan.step_end()
+        for l in range(L):  # the same drift on both plans
+            biases[l] = biases[l] + W.bias_drift(WL, s, l)
+            plan.update_router_bias(l, biases[l])
+            ref.update_router_bias(l, biases[l])
+    torch.cuda.synchronize()
+    sim = oracle.cache_sim(L, E, C, access)
+    np.testing.assert_array_equal(hits, sim["hits"])
+    np.testing.assert_array_equal(misses, sim["misses"])
+    slot_of = np.concatenate([plan.residence(l) for l in range(L)])
+    owner = np.full(C, -1, np.int64)
+    for g, c in enumerate(slot_of):
+        if c >= 0:
+            assert owner[c] == -1
+            owner[c] = g
+    np.testing.assert_array_equal(owner, sim["slot_owner"])
+    assert hits.sum() + misses.sum() == (access >= 0).sum()
+    assert sim["admissions"] >= min(C, len(np.unique(access[access >= 0])))
+    plan.close()
+    ref.close()
+
+
+def test_lfu_admission_counters():
+    """Admission and eviction totals over a run equal the simulator's."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    plan, info = harness.build_plan(WL)
+    C = plan.desc.cache_slots
+    L, E, k, T = WL.layers, WL.experts, WL.top_k, 2
+    access = np.full((WL.steps, L, T * k), -1, np.int32)
+    biases = [info["routers"][l][1].copy() for l in range(L)]
+    plan.stats(-1, reset=True)
+    for s in range(WL.steps):
+        for l in range(L):
+            x = _x(s, l, T)
+            y = torch.empty_like(x)
+            idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+            plan.forward(l, x, y, dbg=dict(topk_idx=idx))
+            torch.cuda.synchronize()
+            d = np.unique(idx.cpu().numpy())
+            access[s, l, : len(d)] = d
+        plan.step_end()
+        for l in range(L):
+            biases[l] = biases[l] + W.bias_drift(WL, s, l)
+            plan.update_router_bias(l, biases[l])
+    tot = plan.stats(-1)
+    sim = oracle.cache_sim(L, E, C, access)
+    assert tot["admissions"] == sim["admissions"]
+    assert tot["evictions"] == sim["evictions"]
+    assert tot["hits"] == sim["hits"].sum() and tot["misses"] == sim["misses"].sum()
+    assert tot["fill_bytes"] == sim["admissions"] * plan_expert_bytes(WL)
+    plan.close()
+
+
+def plan_expert_bytes(wl):
+    return sum(wl.codes_bytes(m) + wl.matrix_shape(m)[0] * (wl.matrix_shape(m)[1] // wl.group) * 2
+               for m in range(3))
