@@ -28,7 +28,8 @@ constexpr int kDecideThreads = 1024;
 struct StepEndArgs {
   int E;
   int64_t LE, C;
-  int step, aging_period;
+  int* step;  // device step counter: this step's number, advanced at the end
+  int aging_period;
   uint32_t* count;
   int32_t* last;
   int32_t* slot_of;
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(kDecideThreads) lfu_decide_kernel(StepEndArgs 
   __shared__ Cand victim;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nm = (int)min((unsigned)a.miss_cap, *a.miss_count);
+  const int step = *a.step;
   // the step's misses in ascending global id (stable among repeats: the key
   // is (id, queue position))
   for (int i = tid; i < nm; i += blockDim.x) {
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kDecideThreads) lfu_decide_kernel(StepEndArgs 
         const int32_t o = a.owner[c];
         if (o < 0) continue;
         const int32_t lo = a.last[o];
-        if (lo == a.step) continue;
+        if (lo == step) continue;
         const Cand x{a.count[o], lo, o};
         if (before(x, best)) best = x;
       }
@@ -141,11 +143,12 @@ __global__ void __launch_bounds__(kDecideThreads) lfu_decide_kernel(StepEndArgs 
     if (slot >= 0) ++nadm;
     __syncthreads();  // tables settled before the next miss
   }
-  if (a.aging_period > 0 && (a.step + 1) % a.aging_period == 0)
+  if (a.aging_period > 0 && (step + 1) % a.aging_period == 0)
     for (int64_t i = tid; i < a.LE; i += blockDim.x) a.count[i] >>= 1;
   if (tid == 0) {
     a.adm[0] = nadm;
     *a.miss_count = 0u;
+    *a.step = step + 1;
   }
 }
 
@@ -172,7 +175,7 @@ cudaError_t moe::lfu_step_end(Plan& p, cudaStream_t s) {
   a.E = d.num_experts;
   a.LE = (int64_t)d.num_layers * d.num_experts;
   a.C = d.cache_slots;
-  a.step = p.step;
+  a.step = &p.ctl->step;
   a.aging_period = d.aging_period;
   a.count = p.lfu_count;
   a.last = p.lfu_last;

@@ -213,7 +213,7 @@ struct ExpertArgs {
   int lfu;
   uint32_t* lfu_count;
   int32_t* lfu_last;
-  int step;
+  const int* step;  // cache step counter (device)
   int32_t* miss_list;
   unsigned* miss_count;
   int miss_cap;
@@ -754,7 +754,7 @@ expert_decode_kernel(ExpertArgs a) {
       for (int d = tid; d < D; d += blockDim.x) {  // distinct experts: no two threads share g
         const int64_t gid = a.ge0 + R.wl_e[d];
         a.lfu_count[gid] += 1u;
-        a.lfu_last[gid] = a.step;
+        a.lfu_last[gid] = *a.step;
         if (d < R.nh) {
           const unsigned mi = atomicAdd(a.miss_count, 1u);
           if ((int)mi < a.miss_cap) a.miss_list[mi] = (int32_t)gid;
@@ -1195,7 +1195,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.lfu = d.cache_policy == MOE_POLICY_LFU;
   a.lfu_count = p.lfu_count;
   a.lfu_last = p.lfu_last;
-  a.step = p.step;
+  a.step = &p.ctl->step;
   a.miss_list = p.miss_list;
   a.miss_count = p.miss_count;
   a.miss_cap = d.num_layers * p.max_distinct;

@@ -64,7 +64,8 @@ enum : uint32_t { kErrTimeout = 1u, kErrBounds = 2u };
 // Control words of the decode path (device).
 struct Ctl {
   unsigned epoch;  // forward counter: bumped by the router kernel, tags the hand-off words
-  unsigned pad[7];
+  int step;        // cache step: read by the forwards, advanced by the step-end kernel
+  unsigned pad[6];
 };
 
 struct Plan {
@@ -123,7 +124,7 @@ struct Plan {
   unsigned* miss_count = nullptr;
   unsigned* adm_list = nullptr;   // step-end: admitted (expert, slot) pairs
   unsigned* adm_count = nullptr;
-  int step = 0;
+  int step = 0;  // host mirror of ctl->step (steps ended through the API)
 
   // statistics and errors
   unsigned long long* stats = nullptr;    // [L][kNumStats]

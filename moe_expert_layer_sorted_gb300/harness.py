@@ -15,11 +15,14 @@ _SC_TORCH = {W.SC_F32: torch.float32, W.SC_BF16: torch.bfloat16, W.SC_F16: torch
 
 
 class ExpertQuantiser:
-    """Generates an expert's fp32 masters on the host, uploads them through a
-    pinned buffer and quantises them on the GPU into canonical codes/scales."""
+    """Generates an expert's fp32 masters (on the host and uploaded through a
+    pinned buffer, or with gpu_gen=True directly on the device by the
+    generator's bit-identical device twin) and quantises them on the GPU into
+    canonical codes/scales."""
 
-    def __init__(self, wl: W.Workload, device="cuda"):
+    def __init__(self, wl: W.Workload, device="cuda", gpu_gen: bool = False):
         self.wl = wl
+        self.gpu_gen = gpu_gen
         self.dev = torch.device(device)
         n = wl.inter * wl.hidden
         self.host = torch.empty(n, dtype=torch.float32).pin_memory()
@@ -33,10 +36,15 @@ class ExpertQuantiser:
         wl = self.wl
         for m in range(3):
             r, c = wl.matrix_shape(m)
-            torch.cuda.current_stream().synchronize()  # the pinned buffer is reused
-            hv = self.host[: r * c].numpy()
-            hv[:] = W.expert_master(wl, layer, e, m).ravel()
-            self.dw[: r * c].copy_(self.host[: r * c], non_blocking=True)
+            if self.gpu_gen:
+                import synth
+                synth.normal_f32_device(W.key(wl.seed, W.TAG_WEIGHT, layer, e, m), r * c, wl.w_sigma,
+                                        self.dw.data_ptr(), torch.cuda.current_stream().cuda_stream)
+            else:
+                torch.cuda.current_stream().synchronize()  # the pinned buffer is reused
+                hv = self.host[: r * c].numpy()
+                hv[:] = W.expert_master(wl, layer, e, m).ravel()
+                self.dw[: r * c].copy_(self.host[: r * c], non_blocking=True)
             quantize(self.dw[: r * c].view(r, c), wl.bits, wl.group, wl.scale_dtype,
                      self.codes[m], self.scales[m])
         torch.cuda.current_stream().synchronize()
@@ -44,7 +52,8 @@ class ExpertQuantiser:
 
 
 def build_plan(wl: W.Workload, *, max_tokens: int | None = None, layers: int | None = None,
-               host_overlap: int = 0, device: int = 0, all_hbm: bool = False, progress=None):
+               host_overlap: int = 0, device: int = 0, all_hbm: bool = False, progress=None,
+               gpu_gen: bool = False):
     """Create a plan for `wl` (first `layers` layers), set its routers and place
     every expert (host-resident ones per the workload).  Returns (plan, info)."""
     L = wl.layers if layers is None else layers
@@ -65,7 +74,7 @@ def build_plan(wl: W.Workload, *, max_tokens: int | None = None, layers: int | N
                 hbm_experts=0 if lfu else L * wl.experts - n_host,
                 cache_slots=int(np.floor(wl.cache_frac * L * wl.experts)) if lfu else 0,
                 host_overlap=host_overlap, device=device)
-    q = ExpertQuantiser(wl, device=f"cuda:{device}")
+    q = ExpertQuantiser(wl, device=f"cuda:{device}", gpu_gen=gpu_gen)
     for l in range(L):
         wr, bias, _ = routers[l]
         plan.set_router(l, wr, bias)

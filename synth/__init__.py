@@ -17,8 +17,11 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
 _LIB = os.path.join(_HERE, "libsynth.so")
+_SRC_GPU = os.path.join(_HERE, "synth_gpu.cu")
+_LIB_GPU = os.path.join(_HERE, "libsynth_gpu.so")
 _lock = threading.Lock()
 _lib = None
+_lib_gpu = None
 
 # stream tags: the first element of every stream key
 TAG_WEIGHT = 1   # (layer, expert, matrix 0=gate 1=up 2=down)
@@ -37,6 +40,43 @@ def build(force: bool = False) -> str:
         subprocess.run(cmd, check=True)
         os.replace(_LIB + ".tmp", _LIB)
     return _LIB
+
+
+def build_gpu(force: bool = False) -> str:
+    """Compile the device twin of the normal draws (synth_gpu.cu) with nvcc."""
+    if force or not os.path.exists(_LIB_GPU) or os.path.getmtime(_LIB_GPU) < os.path.getmtime(_SRC_GPU):
+        cmd = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-Xcompiler", "-fPIC",
+               "-shared", "-o", _LIB_GPU + ".tmp", _SRC_GPU]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB_GPU + ".tmp", _LIB_GPU)
+    return _LIB_GPU
+
+
+def lib_gpu():
+    global _lib_gpu
+    with _lock:
+        if _lib_gpu is None:
+            build_gpu()
+            L = ctypes.CDLL(_LIB_GPU)
+            u64, i64 = ctypes.c_uint64, ctypes.c_int64
+            for f in (L.synth_gpu_normal_f32, L.synth_gpu_normal_bf16):
+                f.argtypes = [u64, u64, i64, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+                f.restype = ctypes.c_int
+            _lib_gpu = L
+    return _lib_gpu
+
+
+def normal_f32_device(k: int, n: int, sigma: float, out_ptr: int, stream_ptr: int = 0, start: int = 0):
+    """The same draws as normal_f32, written by a GPU kernel into device memory."""
+    rc = lib_gpu().synth_gpu_normal_f32(k, start, n, sigma, out_ptr, stream_ptr)
+    if rc:
+        raise RuntimeError(f"synth_gpu_normal_f32 failed ({rc})")
+
+
+def normal_bf16_device(k: int, n: int, sigma: float, out_ptr: int, stream_ptr: int = 0, start: int = 0):
+    rc = lib_gpu().synth_gpu_normal_bf16(k, start, n, sigma, out_ptr, stream_ptr)
+    if rc:
+        raise RuntimeError(f"synth_gpu_normal_bf16 failed ({rc})")
 
 
 def lib():
