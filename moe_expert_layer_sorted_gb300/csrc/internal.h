@@ -112,6 +112,8 @@ struct Plan {
   unsigned long long* hsum = nullptr;  // [maxD][decode T][kpad(I)/16] fp32 sums of 16 h values
   unsigned long long* obuf = nullptr;  // [decode T * k][H] fp32 weighted expert outputs per slot
   float* xsum = nullptr;        // [decode T][H / G] scale-group sums of the layer input
+  uint16_t* pf_h = nullptr;     // prefill: [maxT * k][I] bf16 h per (expert, token) slot, perm order
+  uint16_t* pf_o = nullptr;     // prefill: [maxT * k][H] bf16 weighted expert output per slot
   uint16_t* x_stage = nullptr;  // [maxT][H] for the host-buffer forward
   uint16_t* y_stage = nullptr;
 
@@ -158,5 +160,7 @@ cudaError_t launch_quantize(const float* w, int rows, int cols, int bits, int gr
 cudaError_t decode_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
                            cudaStream_t s, const moe_routing_out* dbg);
 cudaError_t lfu_step_end(Plan& p, cudaStream_t s);
+cudaError_t prefill_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y, cudaStream_t s,
+                            const moe_routing_out* dbg);
 
 }  // namespace moe

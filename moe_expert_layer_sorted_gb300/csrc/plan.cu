@@ -341,7 +341,7 @@ void release(Plan* p) {
   for (auto* b : p->bias) cudaFree(b);
   void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
-                 p->wl_blob, p->ctl, p->hbuf, p->hsum, p->obuf, p->xsum, p->x_stage,
+                 p->wl_blob, p->ctl, p->hbuf, p->hsum, p->obuf, p->pf_h, p->pf_o, p->xsum, p->x_stage,
                  p->y_stage, p->slot_of, p->slot_owner, p->lfu_count, p->lfu_last, p->miss_list,
                  p->miss_count, p->adm_list, p->adm_count, p->stats};
   for (void* v : dev)
@@ -395,7 +395,8 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
 
   // HBM need: arena + routers + tables + scratch, against free memory minus headroom
   const int64_t scratch = maxT * E * 4 + maxT * k * 16 + (E + 1) * 8 + maxD * 32 +
-                          maxD * decT * (I + 256) * 5 + decT * k * H * 8 + 2 * maxT * H * 2 + 4096;
+                          maxD * decT * (I + 256) * 5 + decT * k * H * 8 +
+                          (maxT > kDecodeMaxTokens ? maxT * k * (I + H) * 2 : 0) + 2 * maxT * H * 2 + 4096;
   const int64_t lfu = d.cache_policy == MOE_POLICY_LFU
                           ? LE * 12 + slots * 8 + (int64_t)d.num_layers * maxD * 8
                           : 0;
@@ -471,6 +472,10 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   ALLOC(p->hsum, maxD * decT * (KPI / 16));
   ALLOC(p->obuf, decT * k * H);
   ALLOC(p->xsum, decT * (H / d.group_size));
+  if (maxT > kDecodeMaxTokens) {
+    ALLOC(p->pf_h, maxT * k * I);
+    ALLOC(p->pf_o, maxT * k * H);
+  }
   ALLOC(p->x_stage, maxT * H);
   ALLOC(p->y_stage, maxT * H);
   ALLOC(p->stats, (int64_t)d.num_layers * kNumStats);
@@ -706,7 +711,7 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
   if (p->have_last && p->last_stream != s) CK(p, cudaStreamWaitEvent(s, p->ev_done, 0));
   cudaError_t e;
   if (T <= kDecodeMaxTokens) e = decode_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
-  else return fail(p, MOE_ERR_UNSUPPORTED, "T above the decode path is not built yet");
+  else e = prefill_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
   if (e != cudaSuccess) return cuda_fail(p, e, "forward launch");
   CK(p, cudaEventRecord(p->ev_done, s));
   p->last_stream = s;
