@@ -229,9 +229,12 @@ __global__ void pf_place_kernel(const int32_t* __restrict__ idx, int n, const in
 
 // ------------------------------------------------------------------ tcgen05 GEMM
 
-constexpr int kGemmThreads = 288;  // 4 producer warps, 4 epilogue warps, 1 MMA warp
+constexpr int kProdWarps = 8;                       // producer warps (0..7)
+constexpr int kEpiWarp0 = kProdWarps;               // epilogue warps kEpiWarp0..+3
+constexpr int kMmaWarp = kProdWarps + 4;            // TMEM allocation and MMA issue
+constexpr int kGemmThreads = (kProdWarps + 5) * 32;
 constexpr int kTileM = 128;        // weight rows per unit
-constexpr int kTileN = 256;        // max tokens per unit
+constexpr int kTileN = 192;        // max tokens per unit
 constexpr int kStageK = 64;        // columns per stage (one 128-byte swizzle span of bf16)
 
 struct GemmArgs {
@@ -347,18 +350,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int B, bool GATEUP>
 __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t dsm[];
-  __shared__ __align__(8) unsigned long long fullb[4], emptyb[4], tfull, tempty;
+  __shared__ __align__(8) unsigned long long fullb[4], emptyb[4], tfull[2], tempty[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int tile_prefix[4097];  // units before expert e
   __shared__ int rowsrc[kTileN];     // source row of each token of the current unit (producers)
+  __shared__ float wslot[2][kTileN]; // down: routing weight of each token of a unit (epilogue)
   constexpr int NMAT = GATEUP ? 2 : 1;
+  constexpr int NBUF = GATEUP ? 1 : 2;  // accumulator buffers in TMEM (512 columns either way)
   constexpr uint32_t kATile = kTileM * 128;  // bytes of one 128 x 64 bf16 weight tile
   constexpr uint32_t kBTile = kTileN * 128;
-  constexpr uint32_t kStage = NMAT * kATile + kBTile;
+  // per stage, after the tiles: the stage's code words (each lane's 16-byte
+  // share of each (row tile, matrix)) and scale rows, fetched two stages ahead
+  constexpr uint32_t kCodes = NMAT * 8 * 32 * 16;
+  constexpr uint32_t kScales = NMAT * 8 * 2 * 64;
+  constexpr uint32_t kStage = NMAT * kATile + kBTile + kCodes + kScales;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the dynamic window is 1024-aligned for the swizzled tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   const int E = a.E, NS = a.nstages;
+  int* tile_prefix = reinterpret_cast<int*>(smem + (size_t)NS * kStage);  // [E+1] units before expert e
   const int mtiles = a.rows / kTileM;
   const int S = a.kpad / kStageK;  // stages per unit
   const int nkb = a.kpad / 256;
@@ -374,16 +383,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
     }
     tile_prefix[E] = run;
     for (int q = 0; q < NS; ++q) {
-      mbar_init(smem_addr(&fullb[q]), 128);
+      mbar_init(smem_addr(&fullb[q]), kProdWarps * 32);
       mbar_init(smem_addr(&emptyb[q]), 1);
     }
-    mbar_init(smem_addr(&tfull), 1);
-    mbar_init(smem_addr(&tempty), 128);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(smem_addr(&tfull[q]), 1);
+      mbar_init(smem_addr(&tempty[q]), 128);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 8) {  // TMEM: one 256-column fp32 accumulator per matrix
+  if (warp == kMmaWarp) {  // TMEM: 512 fp32 accumulator columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
-                 "n"(NMAT * 256));
+                 "n"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -408,9 +419,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
     nrows = min(kTileN, ne - nt * kTileN);
   };
 
-  if (warp < 4) {
+  if (warp < kProdWarps) {
     // ------------------------------------------------------------ producers
+    // Per stage: the token rows of stage s+1 are requested (cp.async) and the
+    // codes and scales of stage s+1 loaded into registers while stage s's
+    // weights are dequantised into shared memory, so global latency overlaps
+    // a stage of work.
+    constexpr int NIT = NMAT * 8 / kProdWarps;  // (row tile, matrix) items per warp per stage
     const int g = lane >> 2, tig = lane & 3;
+    uint32_t offc[8];  // swizzled byte offset of the lane's 4 bytes in 16-byte chunk c of rows g, g+8
+#pragma unroll
+    for (int c = 0; c < 8; ++c) offc[c] = (uint32_t)(((c ^ (g & 7)) << 4) + 4 * tig);
+    const bool bfs = a.sdt == MOE_SCALE_BF16;
+    const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
+    const float zb = 128.0f + (float)(1 << (a.bits - 1));
+    const uint32_t negzb2 = pack_bf16x2(-zb, -zb);  // exact: 130, 132 or 136
+    const int64_t ng = a.kpad / G;
+    const uint16_t* bsrc = GATEUP ? a.x : a.hin;
     int gs = 0;  // stages produced so far (all units)
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       int e, mt, n0, nrows;
@@ -418,69 +443,118 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
       const int N = (nrows + 15) & ~15;
       const uint8_t* hb = a.blob_hbm[e];
       const uint8_t* blob = hb ? hb : a.blob_host[e];
-      // token rows of this unit (the previous unit's stages no longer read them:
-      // every one of those stages was produced before this point)
-      asm volatile("bar.sync 2, 128;" ::: "memory");
-      for (int n = tid; n < kTileN; n += 128) {
+      asm volatile("bar.sync 2, %0;" ::"n"(kProdWarps * 32) : "memory");  // previous unit's rows unused now
+      for (int n = tid; n < kTileN; n += kProdWarps * 32) {
         int src = -1;
         if (n < nrows) src = GATEUP ? a.perm[n0 + n] / a.k : n0 + n;
         rowsrc[n] = src;
       }
-      asm volatile("bar.sync 2, 128;" ::: "memory");
-      for (int s = 0; s < S; ++s, ++gs) {
-        const int slot = gs % NS, use = gs / NS;
+      asm volatile("bar.sync 2, %0;" ::"n"(kProdWarps * 32) : "memory");
+      // every global read of stage s2 into its slot: token rows, code words, scale rows
+      auto fetch = [&](int s2) {
+        const int gsl = gs + s2, slot = gsl % NS, use = gsl / NS;
         if (use > 0) mbar_wait(smem_addr(&emptyb[slot]), (uint32_t)(use - 1) & 1u, a.err);
         uint8_t* st = smem + (size_t)slot * kStage;
-        const int kb = s >> 2, q = s & 3;  // 256-column block and quarter
-        // weights: 8 row tiles x NMAT matrices, one (tile, matrix) item per warp step
-        for (int it = warp; it < 8 * NMAT; it += 4) {
-          const int mat = it / 8, rt = it % 8;
-          const int64_t tile = (int64_t)mt * 8 + rt;  // 16-row tile of the matrix
-          const uint8_t* chunk = blob + a.codes[mat] + (tile * nkb + kb) * B * 512;
-          uint32_t w[4];
-          chunk_words<B>(chunk, lane, q, w);
-          // scales of rows g, g+8 for the first and second 32 columns of the stage
-          // (one group when G >= 64, two when G = 32)
-          const uint8_t* sc = blob + a.scales[mat];
-          const int64_t ng = a.kpad / G;
-          const int g0 = (kb * 256 + q * 64) / G, g1 = (kb * 256 + q * 64 + 32) / G;
-          const float s00 = scale_at(sc, (int)((tile * ng + g0) * 16 + g), a.sdt);
-          const float s01 = scale_at(sc, (int)((tile * ng + g0) * 16 + g + 8), a.sdt);
-          const float s10 = g1 == g0 ? s00 : scale_at(sc, (int)((tile * ng + g1) * 16 + g), a.sdt);
-          const float s11 = g1 == g0 ? s01 : scale_at(sc, (int)((tile * ng + g1) * 16 + g + 8), a.sdt);
-          const float zb = 128.0f + (float)(1 << (a.bits - 1));
-          uint8_t* at = st + mat * kATile;
+        uint8_t* bt = st + NMAT * kATile;
+        const int k0 = s2 * kStageK;
+        for (int c = tid; c < N * 8; c += kProdWarps * 32) {
+          const int n = c >> 3, cc = c & 7;
+          const int src = rowsrc[n], col = k0 + cc * 8;
+          uint8_t* dst = bt + sw128(n, cc);
+          if (src >= 0 && col < a.K) cp_async16(dst, bsrc + (int64_t)src * a.K + col);
+          else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        const int kb = s2 >> 2, q = s2 & 3;
+        uint8_t* cw = st + NMAT * kATile + kBTile;
+        uint8_t* sw = cw + kCodes;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {  // pair i: k-step i/4 of the stage, register i%4
-            const uint32_t v = chunk_pair<B>(w, i);
-            const int kk = i >> 2, r = i & 3;
-            const int row = rt * 16 + g + ((r & 1) ? 8 : 0);
-            const int col = kk * 16 + 2 * tig + ((r & 2) ? 8 : 0);
-            const float sc2 = kk < 2 ? ((r & 1) ? s01 : s00) : ((r & 1) ? s11 : s10);
-            const float lo = (bf16f(v & 0xffffu) - zb) * sc2;
-            const float hi = (__uint_as_float(v & 0xffff0000u) - zb) * sc2;
-            *reinterpret_cast<uint32_t*>(at + sw128(row, col >> 3) + ((col & 7) << 1)) = pack_bf16x2(lo, hi);
+        for (int j = 0; j < NIT; ++j) {
+          const int it = warp + kProdWarps * j, mat = it / 8, rt = it % 8;
+          const int64_t tile = (int64_t)mt * 8 + rt;
+          const uint8_t* chunk = blob + a.codes[mat] + (tile * nkb + kb) * B * 512 + lane * 16;
+          uint8_t* dw = cw + (it * 32 + lane) * 16;
+          if constexpr (B == 4) {
+            cp_async16(dw, chunk + q * 512);
+          } else if constexpr (B == 2) {
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dw)),
+                         "l"(chunk + (q >> 1) * 512 + (q & 1) * 8) : "memory");
+          } else {
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+              const int wi = 3 * q + i;
+              asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dw + 4 * i)),
+                           "l"(chunk + (wi >> 2) * 512 + (wi & 3) * 4) : "memory");
+            }
+          }
+          // scale rows of the stage's two 32-column halves (16 rows each); lanes
+          // 0..7 copy the 16-byte pieces
+          if (lane < 8) {
+            const int h = lane >> 2, piece = lane & 3;
+            const int gi = (kb * 256 + q * 64 + 32 * h) / G;
+            if (piece * 16 < 16 * ssz)
+              cp_async16(sw + (it * 2 + h) * 64 + piece * 16,
+                         blob + a.scales[mat] + (tile * ng + gi) * 16 * ssz + piece * 16);
           }
         }
-        // token rows: N x 8 chunks of 16 bytes (rows >= nrows and columns >= K are zero)
-        uint8_t* bt = st + NMAT * kATile;
-        const int k0 = s * kStageK;
-        for (int c = tid; c < N * 8; c += 128) {
-          const int n = c >> 3, cc = c & 7;
-          const int src = rowsrc[n];
-          uint4 v = make_uint4(0, 0, 0, 0);
-          const int col = k0 + cc * 8;
-          if (src >= 0 && col < a.K) {
-            const uint16_t* p = GATEUP ? a.x + (int64_t)src * a.K + col : a.hin + (int64_t)src * a.K + col;
-            v = *reinterpret_cast<const uint4*>(p);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      };
+      fetch(0);
+      if (S > 1) fetch(1);
+      for (int s = 0; s < S; ++s) {
+        const int slot = (gs + s) % NS;
+        // stage s+1's reads may still be in flight; stage s's have landed
+        if (s + 1 < S) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();  // scale rows were fetched by other lanes of this warp
+        uint8_t* st = smem + (size_t)slot * kStage;
+        const uint8_t* cw = st + NMAT * kATile + kBTile;
+        const uint8_t* sw = cw + kCodes;
+#pragma unroll
+        for (int j = 0; j < NIT; ++j) {
+          const int it = warp + kProdWarps * j, mat = it / 8, rt = it % 8;
+          const uint4 wv = *reinterpret_cast<const uint4*>(cw + (it * 32 + lane) * 16);
+          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+          float sc[4];  // rows g, g+8 of halves 0 and 1
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            sc[2 * h] = scale_at(sw + (it * 2 + h) * 64, g, a.sdt);
+            sc[2 * h + 1] = scale_at(sw + (it * 2 + h) * 64, g + 8, a.sdt);
           }
-          *reinterpret_cast<uint4*>(bt + sw128(n, cc)) = v;
+          uint8_t* r0 = st + mat * kATile + (rt * 16 + g) * 128;
+          uint8_t* r1 = r0 + 8 * 128;
+          uint32_t s2[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) s2[h] = pack_bf16x2(sc[h], sc[h]);
+          if (bfs) {  // (128 + u) - zb is exact in bf16; one rounding for the product
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {  // pair i: k-step i/4 of the stage, register i%4
+              const uint32_t v = chunk_pair<B>(w, i);
+              const int kk = i >> 2, r = i & 3;
+              uint32_t t, out;
+              asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(v), "r"(0x3F803F80u), "r"(negzb2));
+              asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(t), "r"(s2[(kk >= 2 ? 2 : 0) + (r & 1)]));
+              *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t v = chunk_pair<B>(w, i);
+              const int kk = i >> 2, r = i & 3;
+              const float sv = sc[(kk >= 2 ? 2 : 0) + (r & 1)];
+              const uint32_t out = pack_bf16x2((bf16f(v & 0xffffu) - zb) * sv, (__uint_as_float(v & 0xffff0000u) - zb) * sv);
+              *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
+            }
+          }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
         mbar_arrive(smem_addr(&fullb[slot]));
+        // two stages ahead, into the slot the tensor core frees while this
+        // stage's successor is dequantised
+        if (s + 2 < S) fetch(s + 2);
       }
+      gs += S;
     }
-  } else if (warp == 8) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       int gs = 0, ui = 0;
@@ -489,11 +563,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
         decode_unit(u, e, mt, n0, nrows);
         const int N = (nrows + 15) & ~15;
         const uint32_t idesc = idesc_bf16(kTileM, N);
-        if (ui > 0) mbar_wait(smem_addr(&tempty), (uint32_t)(ui - 1) & 1u, a.err);  // accumulators free
+        const int buf = ui % NBUF, use = ui / NBUF;
+        if (use > 0) mbar_wait(smem_addr(&tempty[buf]), (uint32_t)(use - 1) & 1u, a.err);  // accumulator free
         tc_fence_after();
+        const uint32_t dacc = tmem + (uint32_t)(buf * 256);
         for (int s = 0; s < S; ++s, ++gs) {
-          const int slot = gs % NS, use = gs / NS;
-          mbar_wait(smem_addr(&fullb[slot]), (uint32_t)use & 1u, a.err);
+          const int slot = gs % NS, su = gs / NS;
+          mbar_wait(smem_addr(&fullb[slot]), (uint32_t)su & 1u, a.err);
           tc_fence_after();
           const uint32_t st = smem_addr(smem + (size_t)slot * kStage);
           const uint32_t bt = st + NMAT * kATile;
@@ -501,26 +577,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
           for (int j = 0; j < kStageK / 16; ++j) {
 #pragma unroll
             for (int mat = 0; mat < NMAT; ++mat)
-              umma_bf16(tmem + mat * 256, smem_desc_sw128(st + mat * kATile + j * 32),
+              umma_bf16(dacc + mat * 256, smem_desc_sw128(st + mat * kATile + j * 32),
                         smem_desc_sw128(bt + j * 32), idesc, (s | j) ? 1u : 0u);
           }
           umma_commit(smem_addr(&emptyb[slot]));  // the stage is free once these MMAs are done
         }
-        umma_commit(smem_addr(&tfull));
+        umma_commit(smem_addr(&tfull[buf]));
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 4-7)
     const int quad = warp & 3;
+    const int et = tid - kEpiWarp0 * 32;  // 0..127
     const int row = quad * 32 + lane;  // weight row within the unit = TMEM lane
     int ui = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
       int e, mt, n0, nrows;
       decode_unit(u, e, mt, n0, nrows);
-      mbar_wait(smem_addr(&tfull), (uint32_t)ui & 1u, a.err);
+      const int buf = ui % NBUF, use = ui / NBUF;
+      if constexpr (!GATEUP) {  // the unit's routing weights, staged while its MMAs run
+        for (int c = et; c < nrows; c += 128) wslot[ui & 1][c] = a.topk_w[a.perm[n0 + c]];
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+      }
+      mbar_wait(smem_addr(&tfull[buf]), (uint32_t)use & 1u, a.err);
       tc_fence_after();
-      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16);
+      const uint32_t ta = tmem + (uint32_t)(buf * 256) + ((uint32_t)(quad * 32) << 16);
       const int64_t ocol = (int64_t)mt * kTileM + row;
       for (int c0 = 0; c0 < nrows; c0 += 16) {
         float v0[16];
@@ -540,22 +622,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             if (c0 + c < nrows) {
-              const int p = n0 + c0 + c;
-              const float w = a.topk_w[a.perm[p]];
-              a.oout[(int64_t)p * a.out_ld + ocol] = __bfloat16_as_ushort(__float2bfloat16_rn(w * v0[c]));
+              const float w = wslot[ui & 1][c0 + c];
+              a.oout[(int64_t)(n0 + c0 + c) * a.out_ld + ocol] = __bfloat16_as_ushort(__float2bfloat16_rn(w * v0[c]));
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_addr(&tempty));
+      mbar_arrive(smem_addr(&tempty[buf]));
     }
   }
   // teardown: the MMA warp frees TMEM once the last accumulator was read
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(NMAT * 256));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(512));
   }
 }
 
@@ -663,7 +744,7 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   int optin = 0;
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device)) != cudaSuccess)
     return e;
-  const size_t static_guess = 24 * 1024;  // barriers, unit table, row sources
+  const size_t static_guess = 8 * 1024;  // barriers, row sources, routing weights
   // gate / up -> h
   {
     GemmArgs a = g;
@@ -677,9 +758,11 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     a.x = x;
     a.hout = p.pf_h;
     a.out_ld = I;
-    const size_t stage = 2 * kTileM * 128 + kTileN * 128;
-    a.nstages = (int)std::min<size_t>(4, ((size_t)optin - static_guess - 1024) / stage);
-    const size_t smem = (size_t)a.nstages * stage + 1024;
+    const size_t stage = 2 * kTileM * 128 + kTileN * 128 + 2 * 8 * 32 * 16 + 2 * 8 * 2 * 64;
+    const size_t table = ((size_t)(E + 1) * 4 + 15) / 16 * 16;
+    a.nstages = (int)std::min<size_t>(4, ((size_t)optin - static_guess - 1024 - table) / stage);
+    if (a.nstages < 3) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)a.nstages * stage + 1024 + table;
     if ((e = launch_gemm<true>(d.weight_bits, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
   // down -> weighted o per slot
@@ -693,9 +776,11 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     a.hin = p.pf_h;
     a.oout = p.pf_o;
     a.out_ld = H;
-    const size_t stage = kTileM * 128 + kTileN * 128;
-    a.nstages = (int)std::min<size_t>(4, ((size_t)optin - static_guess - 1024) / stage);
-    const size_t smem = (size_t)a.nstages * stage + 1024;
+    const size_t stage = kTileM * 128 + kTileN * 128 + 8 * 32 * 16 + 8 * 2 * 64;
+    const size_t table = ((size_t)(E + 1) * 4 + 15) / 16 * 16;
+    a.nstages = (int)std::min<size_t>(4, ((size_t)optin - static_guess - 1024 - table) / stage);
+    if (a.nstages < 3) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)a.nstages * stage + 1024 + table;
     if ((e = launch_gemm<false>(d.weight_bits, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
   pf_combine_kernel<<<4 * p.sms, 256, 0, s>>>(p.pf_o, p.inv, T, H, k, y);
