@@ -41,6 +41,37 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _recorded_traffic(name: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary
+    profiles/<name>.md, if the kernel sources hashed there are unchanged
+    (else None: counters of an older kernel do not describe this one)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    try:
+        kv = {}
+        for line in open(path):
+            if line.startswith("- ") and ": " in line:
+                key, val = line[2:].split(": ", 1)
+                kv[key.strip()] = val.strip()
+        h = hashlib.sha1()
+        for src in kv["sources"].split(","):
+            h.update(open(os.path.join(ROOT, src.strip()), "rb").read())
+        if h.hexdigest() != kv["sources_sha1"]:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def _tensor_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 class ClockSampler:
     """SM clocks and clock-event (throttle) reasons sampled during the timed
     region.  The timed region of a decode step is a few milliseconds, shorter
@@ -357,7 +388,9 @@ def run_ours(args):
                        "cuda_graph": use_graph, "parallelism": "replicas" if ws > 1 else "single GPU"},
             "weight_stream_GBps": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": eff_peak, "unit": "GB/s",
-                         "frac": achieved / eff_peak, "traffic": None,
+                         "frac": achieved / eff_peak, "traffic": _recorded_traffic("expert_decode_kernel_decode_step"),
+                         "traffic_note": "DRAM read+write bytes of one T=4 forward's expert kernel from the ncu "
+                                         "summary in profiles/ (null when the kernel changed since)",
                          "kernel": "router_logits_kernel + expert_decode_kernel (one forward)",
                          "peak_note": f"sum-form roofline: HBM {hbm_peak:.0f} GB/s ({peak_kind}, "
                                       f"MEASURED_PEAKS.json) for HBM bytes + measured host link "
@@ -574,6 +607,83 @@ def run_cached(args):
     plan.close()
 
 
+def run_prefill(args):
+    """Prefill layer (config "prefill"): T = 8192 tokens through one layer
+    (H=4096, I=1024, E=384, top-6, int4 G128 bf16 scales, all experts in HBM)."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    from synth import workloads as W
+    wl = W.WORKLOADS["prefill"]
+    T = args.tokens or wl.tokens[0]
+    dev = torch.device("cuda", 0)
+    tpeak, tkind = _tensor_peak()
+    t0 = time.perf_counter()
+    plan, info = harness.build_plan(wl, gpu_gen=True, max_tokens=T)
+    build_s = time.perf_counter() - t0
+    H, E, k, I = wl.hidden, wl.experts, wl.top_k, wl.inter
+    import synth
+    pool = 3
+    xs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(pool)]
+    for i, x in enumerate(xs):
+        synth.normal_bf16_device(W.key(wl.seed, W.TAG_X, 500 + i, 0), T * H, 1.0, x.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    y = torch.empty_like(xs[0])
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for w in range(args.warmup):
+            plan.forward(0, xs[w % pool], y, stream=stream)
+    stream.synchronize()
+    plan.stats(0, reset=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    ev = []
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.forward(0, xs[i % pool], y, stream=stream)
+            b.record(stream)
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    flops_ffn = 6.0 * T * k * H * I
+    flops_router = 2.0 * T * E * H
+    achieved = (flops_ffn + flops_router) / (ms * 1e-3) / 1e12
+    st = plan.stats(0)
+    # end to end through the host-buffer entry point
+    xh = xs[0].view(torch.int16).cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    e2e = []
+    with torch.cuda.stream(stream):
+        for i in range(max(2, args.steps // 2)):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.forward_host(0, xh, yh, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            e2e.append(a.elapsed_time(b))
+    e2e_ms = float(np.mean(e2e))
+    line = _common_line(
+        args, "MoE prefill tokens/s", T / (ms * 1e-3), "tokens/s", ms,
+        {"workload": wl.desc, "tokens_per_step": T,
+         "l2": "no flush: a step streams ~2.5 GB of weights, far above L2", "cuda_graph": False,
+         "parallelism": "single GPU"},
+        {"tflops": achieved,
+         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                      "frac": achieved / tpeak, "traffic": None,
+                      "kernel": "whole prefill forward (router, grouping, tcgen05 gate/up and down GEMMs, combine)",
+                      "peak_note": f"dense bf16, {tkind} burst figure; FLOPs = 6*T*k*H*I (expert FFNs) + 2*T*E*H (router)"},
+         "cache": {k_: st[k_] for k_ in ("accesses", "hits", "hbm_bytes")},
+         "e2e": {"value": T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                 "d2h_bytes_per_step": T * H * 2},
+         "setup_s": build_s, "gpu_launches": 10 * args.steps, "clocks": ck})
+    print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,8 +693,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=3)
-    ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill"])
     ap.add_argument("--cached-steps", type=int, default=2048)
+    ap.add_argument("--tokens", type=int, default=0, help="prefill: batch size (default 8192)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -594,6 +705,8 @@ def main():
         run_stack(args)
     elif args.workload == "cached":
         run_cached(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 
