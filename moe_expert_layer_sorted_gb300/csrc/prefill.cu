@@ -1,7 +1,7 @@
 // Prefill-batch forward (T > 8 tokens), the shape of "763B MoE in two 96 GB
 // cards" (section "Where the VRAM gap comes from": each token routed to k of
 // E experts, the layer output the routing-weighted sum of the experts'
-// SwiGLU FFNs), as six launches on the caller's stream:
+// SwiGLU FFNs), as a chain of launches on the caller's stream:
 //
 //   1. pf_router_kernel   fp32 router logits in the library's fixed summation
 //                         order (lane j of a warp owns elements 256m + 8j + r;
@@ -14,29 +14,38 @@
 //                         offsets, and the stable (expert, token) order perm /
 //                         inv, one CTA per expert compacting the slots in
 //                         ascending order.
-//   4. pf_gemm_kernel<gate/up>  for every routed (expert, 128 rows of I,
-//                         <= 256 of its tokens): gate and up projections on
-//                         tcgen05 tensor cores with fp32 accumulators in TMEM;
-//                         the epilogue writes h = silu(g) * u (bf16) per
-//                         (token, expert) slot.
-//   5. pf_gemm_kernel<down>  o = Wd h per (expert, 128 rows of H, tokens),
+//   4. pf_gather_kernel   the layer input's rows copied into grouped
+//                         (expert, token) order.
+//   5. pf_gemm_kernel<gate/up>  for every routed (expert, 128 of its tokens,
+//                         128 rows of I): gate and up projections on tcgen05
+//                         tensor cores (M = 128 tokens, N = 128 gate + 128 up
+//                         rows) with fp32 accumulators in TMEM; the epilogue
+//                         writes h = silu(g) * u (bf16) per (token, expert) slot.
+//   6. pf_gemm_kernel<down>  o = Wd h per (expert, 128 tokens, 256 rows of H),
 //                         times the slot's routing weight, bf16 per slot.
-//   6. pf_combine_kernel  y[t] = sum over j ascending of the slot outputs, bf16.
+//   7. pf_combine_kernel  y[t] = sum over j ascending of the slot outputs, bf16.
 //
-// GEMM kernel layout (one CTA of 9 warps per SM, persistent over work units):
-//   warps 0-3  producers: dequantise the unit's 128 weight rows x 64 columns
-//              per stage (int-b codes in the library's fragment-ordered device
-//              layout -> bf16 s*q) and gather its token rows, both into
-//              128-byte-swizzled K-major shared memory tiles;
-//   warp 8     allocates TMEM and (lane 0) issues tcgen05.mma (M = 128 weight
-//              rows, N = tokens, K = 16 per instruction) per stage, releasing
-//              the stage by tcgen05.commit;
-//   warps 4-7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//              lanes 32(w%4)..+31, i.e. weight rows), activation / scaling,
-//              global stores.
+// GEMM kernel layout (one CTA of 23 warps per SM, persistent over work units,
+// consecutive units of an expert sharing its token tile):
+//   warps 0-15  dequantise: warp w turns 16 weight rows x 64 columns per stage
+//               (int-b codes in the library's fragment-ordered device layout ->
+//               bf16 s*q) into a 128-byte-swizzled K-major shared-memory tile;
+//   warp 20     per stage the 128 token rows x 64 columns (one 2-D tensor
+//               copy, 128-byte swizzle);
+//   warp 21     per 256-column code block the unit's codes and scales (bulk
+//               copies from HBM, 16-byte cp.async from pinned host memory);
+//   warp 22     allocates TMEM and (lane 0) issues tcgen05.mma (K = 16 per
+//               instruction) per stage, releasing both stage buffers by
+//               tcgen05.commit; two accumulators of 256 columns alternate
+//               between units;
+//   warps 16-19 epilogue: tcgen05.ld of the accumulator (warp 16+q reads TMEM
+//               lanes 32q..32q+31, i.e. tokens), activation / scaling, 16-byte
+//               global stores.
 // Stages and the accumulator hand-off are tracked by mbarriers; every wait is
 // bounded and latches the plan's error word.
 #include <stdio.h>
+
+#include <cuda.h>
 
 #include <algorithm>
 
@@ -227,32 +236,70 @@ __global__ void pf_place_kernel(const int32_t* __restrict__ idx, int n, const in
   }
 }
 
+// ------------------------------------------------------------------ token rows in (expert, token) order
+
+// xp[p] = x[perm[p] / k]: the layer input gathered into the grouped order, so
+// that every GEMM unit's token rows are one contiguous tile for the TMA.
+__global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int n, int k,
+                                 int H, uint16_t* __restrict__ xp) {
+  const int per = H / 8;  // 16-byte pieces per row
+  const int64_t tot = (int64_t)n * per;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < tot; i += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(i / per), c = (int)(i % per);
+    const int t = perm[p] / k;
+    reinterpret_cast<uint4*>(xp)[i] = reinterpret_cast<const uint4*>(x)[(int64_t)t * per + c];
+  }
+}
+
 // ------------------------------------------------------------------ tcgen05 GEMM
 
-constexpr int kProdWarps = 8;                       // producer warps (0..7)
-constexpr int kEpiWarp0 = kProdWarps;               // epilogue warps kEpiWarp0..+3
-constexpr int kMmaWarp = kProdWarps + 4;            // TMEM allocation and MMA issue
-constexpr int kGemmThreads = (kProdWarps + 5) * 32;
-constexpr int kTileM = 128;        // weight rows per unit
-constexpr int kTileN = 192;        // max tokens per unit
-constexpr int kStageK = 64;        // columns per stage (one 128-byte swizzle span of bf16)
+constexpr int kDqWarps = 16;                  // dequantising warps 0..15, one 16-row weight tile each;
+                                              // warps 16..19: epilogue (TMEM lane quarters 0..3)
+constexpr int kTokWarp = kDqWarps + 4;        // tensor copies of the token rows
+constexpr int kKbWarp = kDqWarps + 5;         // bulk copies of the codes and scales
+constexpr int kMmaWarp = kDqWarps + 6;        // TMEM allocation and tcgen05.mma issue
+constexpr int kGemmThreads = (kDqWarps + 7) * 32;
+constexpr int kTileM = 128;                   // tokens per unit (MMA M = TMEM lanes)
+constexpr int kTileN = 256;                   // weight rows per unit (MMA N)
+constexpr int kStageK = 64;                   // columns per stage (one 128-byte swizzle span of bf16)
+constexpr int kItems = kTileN / 16;           // 16-row weight tiles per unit
+constexpr uint32_t kTokBytes = kTileM * 128;  // one stage of token rows
+constexpr uint32_t kWBytes = kTileN * 128;    // one stage of dequantised weight rows
+constexpr int kMaxRing = 8;
+
+// Position in a ring of mbarrier-tracked buffers: the slot of the next fill
+// and the phase parity that fill completes.  A consumer waits for `phase` on
+// the full barrier; a producer waits for `phase ^ 1` on the empty barrier,
+// which a fresh barrier reports as complete (the first round needs no wait).
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int depth) {
+    if (++slot == depth) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  // parity of the latest fill of slot q (a slot filled at least once)
+  __device__ __forceinline__ uint32_t last_parity(int q) const { return q < slot ? phase : phase ^ 1u; }
+};
 
 struct GemmArgs {
-  int E, k, bits, group, sdt;
-  int K, kpad;       // reduction length (H or I) and its padded length in the device layout
-  int rows;          // weight rows of the matrix (I for gate/up, H for down)
-  int64_t codes[2], scales[2];  // matrix sections in an expert blob (gate, up) or (down, -)
+  int E, k, sdt, G;
+  int K;       // reduction length (H or I): K / 64 stages per unit
+  int nkb;     // 256-column code blocks per 16-row tile in the device layout (kpad / 256)
+  int ng;      // scale groups per row in the device layout (kpad / G)
+  int rtiles;  // weight-row tiles per token tile: I / 128 (gate/up), H / 256 (down)
+  int64_t codes[2], scales[2];  // matrix sections in an expert blob: (gate, up) or (down, -)
   const uint8_t* const* blob_hbm;
   const uint8_t* const* blob_host;
   const int32_t* offsets;  // [E+1]
   const int32_t* perm;     // [T*k] slots in (expert, token) order
-  const uint16_t* x;       // gate/up: layer input [T][H]
-  const uint16_t* hin;     // down: h [T*k][I] per perm position
   const float* topk_w;     // down: routing weight per slot
-  uint16_t* hout;          // gate/up: h [T*k][I]
-  uint16_t* oout;          // down: weighted o [T*k][H]
-  int64_t out_ld;          // row pitch of the output (I or H)
-  int nstages;             // shared-memory ring depth
+  uint16_t* out;           // gate/up: h [T*k][I]; down: weighted o [T*k][H], rows in perm order
+  int64_t out_ld;
+  int nt, nw, nkbs;               // ring depths: token stages, weight stages, code blocks
+  uint32_t kb_codes, kb_scales;   // bytes of one 16-row tile's codes / scales per code block
   uint32_t* err;
 };
 
@@ -289,21 +336,22 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 16 consecutive fp32 columns of the warp's 32 TMEM lanes (one per thread), without the wait
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// byte offset of (row, 16-byte chunk) in a 128-byte-swizzled K-major tile
-__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
-  return (uint32_t)row * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
+// 2-D tiled tensor copy (box of the map) global -> shared, completing on bar
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 // The lane's code words of pairs 16q..16q+15 of a (16-row tile, 256-column
@@ -347,52 +395,70 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Grouped dequant-GEMM over units (expert e, 128 of its tokens, 256 weight rows):
+// D[token][row] = sum_k xg[token][k] * s * q[row][k], the token rows (A, M = 128)
+// a tile of the grouped activations by tensor copy, the weight rows (B, N = 256)
+// dequantised in shared memory.  Gate/up: rows 0-127 of a unit are 128 rows of
+// the gate projection, rows 128-255 the same rows of the up projection, and the
+// epilogue writes h = silu(g) * u.  Down: 256 rows of H, the epilogue writes the
+// slot's routing weight times o.
 template <int B, bool GATEUP>
-__global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
+__global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_constant__ CUtensorMap tok_map,
+                                                                   GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t dsm[];
-  __shared__ __align__(8) unsigned long long fullb[4], emptyb[4], tfull[2], tempty[2];
+  __shared__ __align__(8) unsigned long long tokFull[kMaxRing], tokEmpty[kMaxRing], wFull[kMaxRing],
+      wEmpty[kMaxRing], kbFull[4], kbEmpty[4], tfull[2], tempty[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int rowsrc[kTileN];     // source row of each token of the current unit (producers)
-  __shared__ float wslot[2][kTileN]; // down: routing weight of each token of a unit (epilogue)
-  constexpr int NMAT = GATEUP ? 2 : 1;
-  constexpr int NBUF = GATEUP ? 1 : 2;  // accumulator buffers in TMEM (512 columns either way)
-  constexpr uint32_t kATile = kTileM * 128;  // bytes of one 128 x 64 bf16 weight tile
-  constexpr uint32_t kBTile = kTileN * 128;
-  // per stage, after the tiles: the stage's code words (each lane's 16-byte
-  // share of each (row tile, matrix)) and scale rows, fetched two stages ahead
-  constexpr uint32_t kCodes = NMAT * 8 * 32 * 16;
-  constexpr uint32_t kScales = NMAT * 8 * 2 * 64;
-  constexpr uint32_t kStage = NMAT * kATile + kBTile + kCodes + kScales;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the dynamic window is 1024-aligned for the swizzled tiles
+  // dynamic window (1024-aligned for the swizzled tiles): token ring | weight
+  // ring | code-block ring (codes of the 16 tiles, then their scales) | unit table
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
-  const int E = a.E, NS = a.nstages;
-  int* tile_prefix = reinterpret_cast<int*>(smem + (size_t)NS * kStage);  // [E+1] units before expert e
-  const int mtiles = a.rows / kTileM;
-  const int S = a.kpad / kStageK;  // stages per unit
-  const int nkb = a.kpad / 256;
-  const int G = a.group;
+  uint8_t* tokr = smem;
+  uint8_t* wr = tokr + (size_t)a.nt * kTokBytes;
+  const uint32_t kbBytes = kItems * (a.kb_codes + a.kb_scales);
+  uint8_t* kbr = wr + (size_t)a.nw * kWBytes;
+  int* tile_prefix = reinterpret_cast<int*>(kbr + (size_t)a.nkbs * kbBytes);  // [E+1] units before expert e
+  const int E = a.E;
+  const int S = a.K / kStageK;  // stages per unit
 
-  // unit table: expert e contributes mtiles * ceil(n_e / 256) units
-  if (tid == 0) {
-    int run = 0;
-    for (int e = 0; e < E; ++e) {
-      tile_prefix[e] = run;
-      const int n = a.offsets[e + 1] - a.offsets[e];
-      run += mtiles * ((n + kTileN - 1) / kTileN);
+  // unit table: expert e contributes rtiles * ceil(n_e / 128) units
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int n = e < E ? a.offsets[e + 1] - a.offsets[e] : 0;
+      const int own = a.rtiles * ((n + kTileM - 1) / kTileM);
+      int v = own;  // inclusive prefix over the 32 lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (e < E) tile_prefix[e] = carry + v - own;
+      carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    tile_prefix[E] = run;
-    for (int q = 0; q < NS; ++q) {
-      mbar_init(smem_addr(&fullb[q]), kProdWarps * 32);
-      mbar_init(smem_addr(&emptyb[q]), 1);
+    if (lane == 0) tile_prefix[E] = carry;
+  }
+  if (tid == 0) {
+    for (int q = 0; q < a.nt; ++q) {
+      mbar_init(smem_addr(&tokFull[q]), 1);
+      mbar_init(smem_addr(&tokEmpty[q]), 1);
+    }
+    for (int q = 0; q < a.nw; ++q) {
+      mbar_init(smem_addr(&wFull[q]), kDqWarps);  // one arrival per warp
+      mbar_init(smem_addr(&wEmpty[q]), 1);
+    }
+    for (int q = 0; q < a.nkbs; ++q) {
+      mbar_init(smem_addr(&kbFull[q]), 1);
+      mbar_init(smem_addr(&kbEmpty[q]), kDqWarps);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(smem_addr(&tfull[q]), 1);
-      mbar_init(smem_addr(&tempty[q]), 128);
+      mbar_init(smem_addr(&tempty[q]), 4);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kMmaWarp) {  // TMEM: 512 fp32 accumulator columns
+  if (warp == kMmaWarp) {  // TMEM: two accumulators of 256 fp32 columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
                  "n"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -403,7 +469,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
   const uint32_t tmem = tmem_base;
   const int nunits = tile_prefix[E];
 
-  auto decode_unit = [&](int u, int& e, int& mt, int& n0, int& nrows) {
+  auto decode_unit = [&](int u, int& e, int& rt, int& n0, int& nrows) {
     int lo = 0, hi = E - 1;  // last e with tile_prefix[e] <= u
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -412,224 +478,253 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(GemmArgs a) {
     }
     e = lo;
     const int r = u - tile_prefix[e];
-    mt = r % mtiles;
-    const int nt = r / mtiles;
+    rt = r % a.rtiles;
+    const int tt = r / a.rtiles;
     const int ne = a.offsets[e + 1] - a.offsets[e];
-    n0 = a.offsets[e] + nt * kTileN;
-    nrows = min(kTileN, ne - nt * kTileN);
+    n0 = a.offsets[e] + tt * kTileM;
+    nrows = min(kTileM, ne - tt * kTileM);
   };
 
-  if (warp < kProdWarps) {
-    // ------------------------------------------------------------ producers
-    // Per stage: the token rows of stage s+1 are requested (cp.async) and the
-    // codes and scales of stage s+1 loaded into registers while stage s's
-    // weights are dequantised into shared memory, so global latency overlaps
-    // a stage of work.
-    constexpr int NIT = NMAT * 8 / kProdWarps;  // (row tile, matrix) items per warp per stage
+  if (warp < kDqWarps) {
+    // ------------------------------------------------------------ dequantisers
+    // Warp w turns its 16-row tile of each stage (codes and scales from the
+    // code-block ring) into bf16 s*q, 128-byte-swizzled K-major, in the
+    // weight ring: rows 16w..16w+15 of the unit's 256.
     const int g = lane >> 2, tig = lane & 3;
     uint32_t offc[8];  // swizzled byte offset of the lane's 4 bytes in 16-byte chunk c of rows g, g+8
 #pragma unroll
     for (int c = 0; c < 8; ++c) offc[c] = (uint32_t)(((c ^ (g & 7)) << 4) + 4 * tig);
     const bool bfs = a.sdt == MOE_SCALE_BF16;
     const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
-    const float zb = 128.0f + (float)(1 << (a.bits - 1));
+    const float zb = 128.0f + (float)(1 << (B - 1));
     const uint32_t negzb2 = pack_bf16x2(-zb, -zb);  // exact: 130, 132 or 136
-    const int64_t ng = a.kpad / G;
-    const uint16_t* bsrc = GATEUP ? a.x : a.hin;
-    int gs = 0;  // stages produced so far (all units)
+    const int lg_g = 31 - __clz(a.G);                      // G = 32, 64 or 128
+    const int lg_srow = ssz == 4 ? 6 : 5;                  // bytes of 16 scales = 1 << lg_srow
+    RingPos kp, wp;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-      int e, mt, n0, nrows;
-      decode_unit(u, e, mt, n0, nrows);
-      const int N = (nrows + 15) & ~15;
-      const uint8_t* hb = a.blob_hbm[e];
-      const uint8_t* blob = hb ? hb : a.blob_host[e];
-      asm volatile("bar.sync 2, %0;" ::"n"(kProdWarps * 32) : "memory");  // previous unit's rows unused now
-      for (int n = tid; n < kTileN; n += kProdWarps * 32) {
-        int src = -1;
-        if (n < nrows) src = GATEUP ? a.perm[n0 + n] / a.k : n0 + n;
-        rowsrc[n] = src;
-      }
-      asm volatile("bar.sync 2, %0;" ::"n"(kProdWarps * 32) : "memory");
-      // every global read of stage s2 into its slot: token rows, code words, scale rows
-      auto fetch = [&](int s2) {
-        const int gsl = gs + s2, slot = gsl % NS, use = gsl / NS;
-        if (use > 0) mbar_wait(smem_addr(&emptyb[slot]), (uint32_t)(use - 1) & 1u, a.err);
-        uint8_t* st = smem + (size_t)slot * kStage;
-        uint8_t* bt = st + NMAT * kATile;
-        const int k0 = s2 * kStageK;
-        for (int c = tid; c < N * 8; c += kProdWarps * 32) {
-          const int n = c >> 3, cc = c & 7;
-          const int src = rowsrc[n], col = k0 + cc * 8;
-          uint8_t* dst = bt + sw128(n, cc);
-          if (src >= 0 && col < a.K) cp_async16(dst, bsrc + (int64_t)src * a.K + col);
-          else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-        }
-        const int kb = s2 >> 2, q = s2 & 3;
-        uint8_t* cw = st + NMAT * kATile + kBTile;
-        uint8_t* sw = cw + kCodes;
-#pragma unroll
-        for (int j = 0; j < NIT; ++j) {
-          const int it = warp + kProdWarps * j, mat = it / 8, rt = it % 8;
-          const int64_t tile = (int64_t)mt * 8 + rt;
-          const uint8_t* chunk = blob + a.codes[mat] + (tile * nkb + kb) * B * 512 + lane * 16;
-          uint8_t* dw = cw + (it * 32 + lane) * 16;
-          if constexpr (B == 4) {
-            cp_async16(dw, chunk + q * 512);
-          } else if constexpr (B == 2) {
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dw)),
-                         "l"(chunk + (q >> 1) * 512 + (q & 1) * 8) : "memory");
-          } else {
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-              const int wi = 3 * q + i;
-              asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dw + 4 * i)),
-                           "l"(chunk + (wi >> 2) * 512 + (wi & 3) * 4) : "memory");
-            }
-          }
-          // scale rows of the stage's two 32-column halves (16 rows each); lanes
-          // 0..7 copy the 16-byte pieces
-          if (lane < 8) {
-            const int h = lane >> 2, piece = lane & 3;
-            const int gi = (kb * 256 + q * 64 + 32 * h) / G;
-            if (piece * 16 < 16 * ssz)
-              cp_async16(sw + (it * 2 + h) * 64 + piece * 16,
-                         blob + a.scales[mat] + (tile * ng + gi) * 16 * ssz + piece * 16);
-          }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-      };
-      fetch(0);
-      if (S > 1) fetch(1);
       for (int s = 0; s < S; ++s) {
-        const int slot = (gs + s) % NS;
-        // stage s+1's reads may still be in flight; stage s's have landed
-        if (s + 1 < S) asm volatile("cp.async.wait_group 1;" ::: "memory");
-        else asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncwarp();  // scale rows were fetched by other lanes of this warp
-        uint8_t* st = smem + (size_t)slot * kStage;
-        const uint8_t* cw = st + NMAT * kATile + kBTile;
-        const uint8_t* sw = cw + kCodes;
+        const int q = s & 3, kslot = kp.slot, wslot = wp.slot;
+        if (q == 0) mbar_wait(smem_addr(&kbFull[kslot]), kp.phase, a.err);
+        mbar_wait(smem_addr(&wEmpty[wslot]), wp.phase ^ 1u, a.err);
+        const uint8_t* kb = kbr + (size_t)kslot * kbBytes;
+        uint32_t w[4];
+        chunk_words<B>(kb + warp * a.kb_codes, lane, q, w);
+        const uint8_t* sitem = kb + kItems * a.kb_codes + warp * a.kb_scales;
+        float sc[4];  // rows g, g+8 of the stage's column halves 0 and 1
 #pragma unroll
-        for (int j = 0; j < NIT; ++j) {
-          const int it = warp + kProdWarps * j, mat = it / 8, rt = it % 8;
-          const uint4 wv = *reinterpret_cast<const uint4*>(cw + (it * 32 + lane) * 16);
-          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-          float sc[4];  // rows g, g+8 of halves 0 and 1
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            sc[2 * h] = scale_at(sw + (it * 2 + h) * 64, g, a.sdt);
-            sc[2 * h + 1] = scale_at(sw + (it * 2 + h) * 64, g + 8, a.sdt);
-          }
-          uint8_t* r0 = st + mat * kATile + (rt * 16 + g) * 128;
-          uint8_t* r1 = r0 + 8 * 128;
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t* srow = sitem + (((q * 64 + 32 * h) >> lg_g) << lg_srow);
+          sc[2 * h] = scale_at(srow, g, a.sdt);
+          sc[2 * h + 1] = scale_at(srow, g + 8, a.sdt);
+        }
+        uint8_t* r0 = wr + (size_t)wslot * kWBytes + (warp * 16 + g) * 128;
+        uint8_t* r1 = r0 + 8 * 128;
+        if (bfs) {  // (128 + u) - zb is exact in bf16; one rounding for the product
           uint32_t s2[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) s2[h] = pack_bf16x2(sc[h], sc[h]);
-          if (bfs) {  // (128 + u) - zb is exact in bf16; one rounding for the product
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {  // pair i: k-step i/4 of the stage, register i%4
-              const uint32_t v = chunk_pair<B>(w, i);
-              const int kk = i >> 2, r = i & 3;
-              uint32_t t, out;
-              asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(v), "r"(0x3F803F80u), "r"(negzb2));
-              asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(t), "r"(s2[(kk >= 2 ? 2 : 0) + (r & 1)]));
-              *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const uint32_t v = chunk_pair<B>(w, i);
-              const int kk = i >> 2, r = i & 3;
-              const float sv = sc[(kk >= 2 ? 2 : 0) + (r & 1)];
-              const uint32_t out = pack_bf16x2((bf16f(v & 0xffffu) - zb) * sv, (__uint_as_float(v & 0xffff0000u) - zb) * sv);
-              *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
-            }
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
-        mbar_arrive(smem_addr(&fullb[slot]));
-        // two stages ahead, into the slot the tensor core frees while this
-        // stage's successor is dequantised
-        if (s + 2 < S) fetch(s + 2);
-      }
-      gs += S;
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      int gs = 0, ui = 0;
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
-        int e, mt, n0, nrows;
-        decode_unit(u, e, mt, n0, nrows);
-        const int N = (nrows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(kTileM, N);
-        const int buf = ui % NBUF, use = ui / NBUF;
-        if (use > 0) mbar_wait(smem_addr(&tempty[buf]), (uint32_t)(use - 1) & 1u, a.err);  // accumulator free
-        tc_fence_after();
-        const uint32_t dacc = tmem + (uint32_t)(buf * 256);
-        for (int s = 0; s < S; ++s, ++gs) {
-          const int slot = gs % NS, su = gs / NS;
-          mbar_wait(smem_addr(&fullb[slot]), (uint32_t)su & 1u, a.err);
-          tc_fence_after();
-          const uint32_t st = smem_addr(smem + (size_t)slot * kStage);
-          const uint32_t bt = st + NMAT * kATile;
-#pragma unroll
-          for (int j = 0; j < kStageK / 16; ++j) {
-#pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat)
-              umma_bf16(dacc + mat * 256, smem_desc_sw128(st + mat * kATile + j * 32),
-                        smem_desc_sw128(bt + j * 32), idesc, (s | j) ? 1u : 0u);
-          }
-          umma_commit(smem_addr(&emptyb[slot]));  // the stage is free once these MMAs are done
-        }
-        umma_commit(smem_addr(&tfull[buf]));
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue (warps 4-7)
-    const int quad = warp & 3;
-    const int et = tid - kEpiWarp0 * 32;  // 0..127
-    const int row = quad * 32 + lane;  // weight row within the unit = TMEM lane
-    int ui = 0;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
-      int e, mt, n0, nrows;
-      decode_unit(u, e, mt, n0, nrows);
-      const int buf = ui % NBUF, use = ui / NBUF;
-      if constexpr (!GATEUP) {  // the unit's routing weights, staged while its MMAs run
-        for (int c = et; c < nrows; c += 128) wslot[ui & 1][c] = a.topk_w[a.perm[n0 + c]];
-        asm volatile("bar.sync 3, 128;" ::: "memory");
-      }
-      mbar_wait(smem_addr(&tfull[buf]), (uint32_t)use & 1u, a.err);
-      tc_fence_after();
-      const uint32_t ta = tmem + (uint32_t)(buf * 256) + ((uint32_t)(quad * 32) << 16);
-      const int64_t ocol = (int64_t)mt * kTileM + row;
-      for (int c0 = 0; c0 < nrows; c0 += 16) {
-        float v0[16];
-        tmem_ld16(ta + c0, v0);
-        if constexpr (GATEUP) {
-          float v1[16];
-          tmem_ld16(ta + 256 + c0, v1);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c0 + c < nrows) {
-              const float gv = v0[c], uv = v1[c];
-              const float h = gv / (1.0f + expf(-gv)) * uv;
-              a.hout[(int64_t)(n0 + c0 + c) * a.out_ld + ocol] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
-            }
+          for (int i = 0; i < 16; ++i) {  // pair i: k-step i/4 of the stage, register i%4
+            const uint32_t v = chunk_pair<B>(w, i);
+            const int kk = i >> 2, r = i & 3;
+            uint32_t t, out;
+            asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(v), "r"(0x3F803F80u), "r"(negzb2));
+            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(t), "r"(s2[(kk >= 2 ? 2 : 0) + (r & 1)]));
+            *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c0 + c < nrows) {
-              const float w = wslot[ui & 1][c0 + c];
-              a.oout[(int64_t)(n0 + c0 + c) * a.out_ld + ocol] = __bfloat16_as_ushort(__float2bfloat16_rn(w * v0[c]));
-            }
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t v = chunk_pair<B>(w, i);
+            const int kk = i >> 2, r = i & 3;
+            const float sv = sc[(kk >= 2 ? 2 : 0) + (r & 1)];
+            const uint32_t out = pack_bf16x2((bf16f(v & 0xffffu) - zb) * sv, (__uint_as_float(v & 0xffff0000u) - zb) * sv);
+            *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
+          }
+        }
+        // every lane's stores visible to the tensor core, then one arrival for the warp
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&wFull[wslot]));
+        if (q == 3 || s == S - 1) {  // the warp reads the code block no more
+          if (lane == 0) mbar_arrive(smem_addr(&kbEmpty[kslot]));
+          kp.next(a.nkbs);
+        }
+        wp.next(a.nw);
+      }
+    }
+  } else if (warp == kKbWarp) {
+    // ------------------------------------------------------------ code blocks
+    // Per 256-column code block (4 stages) of a unit: the 16 tiles' codes and
+    // scales, one bulk copy each from HBM, 16-byte cp.async by all lanes from
+    // pinned host memory; as far ahead as the ring allows.
+    const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
+    const int gpk = 256 >> (31 - __clz(a.G));  // scale groups per code block
+    const int nkbu = (S + 3) >> 2;              // code blocks per unit
+    RingPos kp;
+    int nkfill = 0;
+    uint32_t hostmask = 0;  // slots last written by cp.async
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      int e, rt, n0, nrows;
+      decode_unit(u, e, rt, n0, nrows);
+      const uint8_t* hb = a.blob_hbm[e];
+      const bool host = hb == nullptr;
+      const uint8_t* blob = host ? a.blob_host[e] : hb;
+      for (int kb = 0; kb < nkbu; ++kb) {
+        const int slot = kp.slot;
+        mbar_wait(smem_addr(&kbEmpty[slot]), kp.phase ^ 1u, a.err);
+        uint8_t* dst = kbr + (size_t)slot * kbBytes;
+        const uint32_t bar = smem_addr(&kbFull[slot]);
+        if (!host) {
+          if (lane == 0) {
+            if ((hostmask >> slot) & 1u) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(bar, kbBytes);
+          }
+          __syncwarp();
+          if (lane < kItems) {
+            const int mat = GATEUP ? (lane >> 3) : 0;
+            const int64_t t16 = GATEUP ? (int64_t)rt * 8 + (lane & 7) : (int64_t)rt * 16 + lane;
+            bulk_g2s(smem_addr(dst + lane * a.kb_codes), blob + a.codes[mat] + (t16 * a.nkb + kb) * B * 512,
+                     a.kb_codes, bar);
+            bulk_g2s(smem_addr(dst + kItems * a.kb_codes + lane * a.kb_scales),
+                     blob + a.scales[mat] + (t16 * a.ng + (int64_t)kb * gpk) * 16 * ssz, a.kb_scales, bar);
+          }
+          hostmask &= ~(1u << slot);
+        } else {
+          for (int it = 0; it < kItems; ++it) {
+            const int mat = GATEUP ? (it >> 3) : 0;
+            const int64_t t16 = GATEUP ? (int64_t)rt * 8 + (it & 7) : (int64_t)rt * 16 + it;
+            const uint8_t* cs = blob + a.codes[mat] + (t16 * a.nkb + kb) * B * 512;
+            const uint8_t* ss = blob + a.scales[mat] + (t16 * a.ng + (int64_t)kb * gpk) * 16 * ssz;
+            for (uint32_t c = lane; c < a.kb_codes / 16; c += 32) cp_async16(dst + it * a.kb_codes + c * 16, cs + c * 16);
+            for (uint32_t c = lane; c < a.kb_scales / 16; c += 32)
+              cp_async16(dst + kItems * a.kb_codes + it * a.kb_scales + c * 16, ss + c * 16);
+          }
+          cp_async_mbar_arrive(bar);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar);
+          hostmask |= 1u << slot;
+        }
+        kp.next(a.nkbs);
+        ++nkfill;
+      }
+    }
+    cp_async_wait<0>();
+    // no copy of this CTA is in flight when it exits: the last fill of every slot has landed
+    if (lane == 0)
+      for (int q = 0; q < a.nkbs && q < nkfill; ++q) mbar_drain(smem_addr(&kbFull[q]), kp.last_parity(q));
+    __syncwarp();
+  } else if (warp == kTokWarp) {
+    // ------------------------------------------------------------ token rows
+    // Per stage: the unit's 128 token rows x 64 columns by one tensor copy.
+    RingPos tp;
+    int ntfill = 0;
+    if (lane == 0) {
+      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+        int e, rt, n0, nrows;
+        decode_unit(u, e, rt, n0, nrows);
+        for (int s = 0; s < S; ++s) {
+          const int slot = tp.slot;
+          mbar_wait(smem_addr(&tokEmpty[slot]), tp.phase ^ 1u, a.err);
+          const uint32_t bar = smem_addr(&tokFull[slot]);
+          mbar_arrive_expect_tx(bar, kTokBytes);
+          tma_load_2d(smem_addr(tokr + (size_t)slot * kTokBytes), &tok_map, s * kStageK, n0, bar);
+          tp.next(a.nt);
+          ++ntfill;
+        }
+      }
+      for (int q = 0; q < a.nt && q < ntfill; ++q) mbar_drain(smem_addr(&tokFull[q]), tp.last_parity(q));
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTileM, kTileN);
+      RingPos tp, wp;
+      int ui = 0;
+      for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
+        const int buf = ui & 1;
+        mbar_wait(smem_addr(&tempty[buf]), ((uint32_t)(ui >> 1) & 1u) ^ 1u, a.err);  // accumulator free
+        tc_fence_after();
+        const uint32_t dacc = tmem + (uint32_t)(buf * 256);
+        for (int s = 0; s < S; ++s) {
+          const int ts = tp.slot, wsl = wp.slot;
+          mbar_wait(smem_addr(&tokFull[ts]), tp.phase, a.err);
+          mbar_wait(smem_addr(&wFull[wsl]), wp.phase, a.err);
+          tc_fence_after();
+          const uint32_t at = smem_addr(tokr + (size_t)ts * kTokBytes);
+          const uint32_t bt = smem_addr(wr + (size_t)wsl * kWBytes);
+#pragma unroll
+          for (int j = 0; j < kStageK / 16; ++j)
+            umma_bf16(dacc, smem_desc_sw128(at + j * 32), smem_desc_sw128(bt + j * 32), idesc, (s | j) ? 1u : 0u);
+          umma_commit(smem_addr(&tokEmpty[ts]));  // both stages are free once these MMAs are done
+          umma_commit(smem_addr(&wEmpty[wsl]));
+          tp.next(a.nt);
+          wp.next(a.nw);
+        }
+        umma_commit(smem_addr(&tfull[buf]));
+      }
+      // the last MMAs have completed before TMEM is released
+      for (int j = max(0, ui - 2); j < ui; ++j) mbar_drain(smem_addr(&tfull[j & 1]), (uint32_t)(j >> 1) & 1u);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 16-19)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // token within the unit = TMEM lane
+    int ui = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
+      int e, rt, n0, nrows;
+      decode_unit(u, e, rt, n0, nrows);
+      const int buf = ui & 1;
+      const bool live = row < nrows;
+      float wgt = 0.0f;
+      if (!GATEUP && live) wgt = a.topk_w[a.perm[n0 + row]];
+      mbar_wait(smem_addr(&tfull[buf]), (uint32_t)(ui >> 1) & 1u, a.err);
+      tc_fence_after();
+      const uint32_t ta = tmem + (uint32_t)(buf * 256) + ((uint32_t)(quad * 32) << 16);
+      uint16_t* orow = a.out + (int64_t)(n0 + row) * a.out_ld;
+      if constexpr (GATEUP) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+          uint32_t gv[16], uv[16];
+          tmem_ld16_nowait(ta + c0, gv);
+          tmem_ld16_nowait(ta + 128 + c0, uv);
+          tmem_wait_ld();
+          uint32_t hp[8];
+#pragma unroll
+          for (int c = 0; c < 16; c += 2) {
+            const float g0 = __uint_as_float(gv[c]), g1 = __uint_as_float(gv[c + 1]);
+            const float h0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(uv[c]);
+            const float h1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(uv[c + 1]);
+            hp[c >> 1] = pack_bf16x2(h0, h1);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + rt * 128 + c0);
+            dst[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            dst[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16_nowait(ta + c0, v);
+          tmem_wait_ld();
+          uint32_t op[8];
+#pragma unroll
+          for (int c = 0; c < 16; c += 2)
+            op[c >> 1] = pack_bf16x2(wgt * __uint_as_float(v[c]), wgt * __uint_as_float(v[c + 1]));
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + rt * 256 + c0);
+            dst[0] = make_uint4(op[0], op[1], op[2], op[3]);
+            dst[1] = make_uint4(op[4], op[5], op[6], op[7]);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_addr(&tempty[buf]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tempty[buf]));
     }
   }
   // teardown: the MMA warp frees TMEM once the last accumulator was read
@@ -696,18 +791,75 @@ __global__ void pf_stats_kernel(const int32_t* __restrict__ counts, int E, const
 }
 
 template <bool GATEUP>
-cudaError_t launch_gemm(int bits, const GemmArgs& a, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_gemm(int bits, const CUtensorMap& map, const GemmArgs& a, int grid, size_t smem, cudaStream_t s) {
   const void* fn = bits == 2   ? (const void*)pf_gemm_kernel<2, GATEUP>
                    : bits == 3 ? (const void*)pf_gemm_kernel<3, GATEUP>
                                : (const void*)pf_gemm_kernel<4, GATEUP>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   switch (bits) {
-    case 2: pf_gemm_kernel<2, GATEUP><<<grid, kGemmThreads, smem, s>>>(a); break;
-    case 3: pf_gemm_kernel<3, GATEUP><<<grid, kGemmThreads, smem, s>>>(a); break;
-    default: pf_gemm_kernel<4, GATEUP><<<grid, kGemmThreads, smem, s>>>(a); break;
+    case 2: pf_gemm_kernel<2, GATEUP><<<grid, kGemmThreads, smem, s>>>(map, a); break;
+    case 3: pf_gemm_kernel<3, GATEUP><<<grid, kGemmThreads, smem, s>>>(map, a); break;
+    default: pf_gemm_kernel<4, GATEUP><<<grid, kGemmThreads, smem, s>>>(map, a); break;
   }
   return cudaGetLastError();
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows][cols] read as boxes of 128
+// rows x 64 columns, 128-byte swizzled (rows past the end read as zero).
+cudaError_t rows_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int cols) {
+  const EncodeTiledFn f = encode_tiled();
+  if (!f) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kStageK, (cuuint32_t)kTileM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Ring depths within the opt-in shared memory: two code blocks, three weight
+// stages (two if three leave fewer than three token stages), and as many
+// token stages as fit (at most kMaxRing).
+bool ring_depths(GemmArgs& a, int optin, int E) {
+  const size_t kb = (size_t)kItems * (a.kb_codes + a.kb_scales);
+  const size_t fixed = 2048 /* static */ + 1024 /* alignment */ + ((size_t)(E + 1) * 4 + 15) / 16 * 16;
+  if ((size_t)optin < fixed + 2 * kb) return false;
+  const size_t room = (size_t)optin - fixed - 2 * kb;
+  a.nkbs = 2;
+  for (int nw = 3; nw >= 2; --nw) {
+    if (room < (size_t)nw * kWBytes) continue;
+    const int nt = (int)std::min<size_t>(kMaxRing, (room - (size_t)nw * kWBytes) / kTokBytes);
+    if (nt >= 3 || (nw == 2 && nt >= 2)) {
+      a.nw = nw;
+      a.nt = nt;
+      return true;
+    }
+  }
+  return false;
+}
+
+size_t gemm_smem(const GemmArgs& a, int E) {
+  return 1024 + (size_t)a.nt * kTokBytes + (size_t)a.nw * kWBytes +
+         (size_t)a.nkbs * kItems * (a.kb_codes + a.kb_scales) + (size_t)(E + 1) * 4;
 }
 
 }  // namespace
@@ -728,60 +880,60 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   pf_place_kernel<<<E, 1024, 0, s>>>(p.topk_idx, n, p.offsets, p.perm, p.inv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+  // token rows in grouped order, into the o buffer (free until the down projection)
+  pf_gather_kernel<<<4 * p.sms, 256, 0, s>>>(x, p.perm, n, k, H, p.pf_o);
+
   const int64_t ge0 = (int64_t)layer * E;
+  const int G = d.group_size;
+  const int ssz = d.scale_dtype == MOE_SCALE_F32 ? 4 : 2;
   GemmArgs g{};
   g.E = E;
   g.k = k;
-  g.bits = d.weight_bits;
-  g.group = d.group_size;
   g.sdt = d.scale_dtype;
+  g.G = G;
   g.blob_hbm = p.blob_hbm + ge0;
   g.blob_host = p.blob_host + ge0;
   g.offsets = p.offsets;
   g.perm = p.perm;
   g.topk_w = p.topk_w;
   g.err = p.err_dev;
+  g.kb_codes = (uint32_t)d.weight_bits * 512u;
+  g.kb_scales = (uint32_t)((256 / G) * 16 * ssz);
   int optin = 0;
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device)) != cudaSuccess)
     return e;
-  const size_t static_guess = 8 * 1024;  // barriers, row sources, routing weights
+  if (!ring_depths(g, optin, E)) return cudaErrorInvalidConfiguration;
+  const size_t smem = gemm_smem(g, E);
+  CUtensorMap map;
   // gate / up -> h
   {
     GemmArgs a = g;
     a.K = H;
-    a.kpad = p.lay.m[0].kpad;
-    a.rows = I;
+    a.nkb = p.lay.m[0].kpad / 256;
+    a.ng = p.lay.m[0].kpad / G;
+    a.rtiles = I / 128;
     a.codes[0] = p.lay.m[0].codes_off;
     a.scales[0] = p.lay.m[0].scales_off;
     a.codes[1] = p.lay.m[1].codes_off;
     a.scales[1] = p.lay.m[1].scales_off;
-    a.x = x;
-    a.hout = p.pf_h;
+    a.out = p.pf_h;
     a.out_ld = I;
-    const size_t stage = 2 * kTileM * 128 + kTileN * 128 + 2 * 8 * 32 * 16 + 2 * 8 * 2 * 64;
-    const size_t table = ((size_t)(E + 1) * 4 + 15) / 16 * 16;
-    a.nstages = (int)std::min<size_t>(4, ((size_t)optin - static_guess - 1024 - table) / stage);
-    if (a.nstages < 3) return cudaErrorInvalidConfiguration;
-    const size_t smem = (size_t)a.nstages * stage + 1024 + table;
-    if ((e = launch_gemm<true>(d.weight_bits, a, p.sms, smem, s)) != cudaSuccess) return e;
+    if ((e = rows_map(&map, p.pf_o, n, H)) != cudaSuccess) return e;
+    if ((e = launch_gemm<true>(d.weight_bits, map, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
   // down -> weighted o per slot
   {
     GemmArgs a = g;
     a.K = I;
-    a.kpad = p.lay.m[2].kpad;
-    a.rows = H;
+    a.nkb = p.lay.m[2].kpad / 256;
+    a.ng = p.lay.m[2].kpad / G;
+    a.rtiles = H / 256;
     a.codes[0] = p.lay.m[2].codes_off;
     a.scales[0] = p.lay.m[2].scales_off;
-    a.hin = p.pf_h;
-    a.oout = p.pf_o;
+    a.out = p.pf_o;
     a.out_ld = H;
-    const size_t stage = kTileM * 128 + kTileN * 128 + 8 * 32 * 16 + 8 * 2 * 64;
-    const size_t table = ((size_t)(E + 1) * 4 + 15) / 16 * 16;
-    a.nstages = (int)std::min<size_t>(4, ((size_t)optin - static_guess - 1024 - table) / stage);
-    if (a.nstages < 3) return cudaErrorInvalidConfiguration;
-    const size_t smem = (size_t)a.nstages * stage + 1024 + table;
-    if ((e = launch_gemm<false>(d.weight_bits, a, p.sms, smem, s)) != cudaSuccess) return e;
+    if ((e = rows_map(&map, p.pf_h, n, I)) != cudaSuccess) return e;
+    if ((e = launch_gemm<false>(d.weight_bits, map, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
   pf_combine_kernel<<<4 * p.sms, 256, 0, s>>>(p.pf_o, p.inv, T, H, k, y);
   pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, p.blob_hbm + ge0, p.stats + (int64_t)layer * kNumStats,
