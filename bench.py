@@ -389,9 +389,10 @@ def run_ours(args):
             "weight_stream_GBps": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": eff_peak, "unit": "GB/s",
                          "frac": achieved / eff_peak, "traffic": _recorded_traffic("expert_decode_kernel_decode_step"),
-                         "traffic_note": "DRAM read+write bytes of one T=4 forward's expert kernel from the ncu "
-                                         "summary in profiles/ (null when the kernel changed since)",
-                         "kernel": "router_logits_kernel + expert_decode_kernel (one forward)",
+                         "traffic_note": "DRAM read+write bytes of one step's three expert-kernel launches "
+                                         "(T = 1, 4, 6) from the ncu summary in profiles/, against the step's "
+                                         "hbm_bytes_per_step (null when the kernel changed since)",
+                         "kernel": "router_logits_kernel + expert_decode_kernel (one step: forwards at T = 1, 4, 6)",
                          "peak_note": f"sum-form roofline: HBM {hbm_peak:.0f} GB/s ({peak_kind}, "
                                       f"MEASURED_PEAKS.json) for HBM bytes + measured host link "
                                       f"{link_gbs:.1f} GB/s for host bytes",
@@ -673,7 +674,9 @@ def run_prefill(args):
          "parallelism": "single GPU"},
         {"tflops": achieved,
          "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                      "frac": achieved / tpeak, "traffic": None,
+                      "frac": achieved / tpeak, "traffic": _recorded_traffic("pf_gemm_kernel_prefill_T8192"),
+                      "traffic_note": "DRAM read+write bytes of one gate/up GEMM launch (the dominant kernel) from "
+                                      "the ncu summary in profiles/ (null when the kernel changed since)",
                       "kernel": "whole prefill forward (router, grouping, tcgen05 gate/up and down GEMMs, combine)",
                       "peak_note": f"dense bf16, {tkind} burst figure; FLOPs = 6*T*k*H*I (expert FFNs) + 2*T*E*H (router)"},
          "cache": {k_: st[k_] for k_ in ("accesses", "hits", "hbm_bytes")},
