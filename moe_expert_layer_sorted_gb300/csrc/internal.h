@@ -34,6 +34,7 @@ constexpr int kBlockK = 256;
 constexpr int kBRows = 64;           // rows of the down projection per B work unit
 constexpr int kDecodeMaxTokens = 8;  // forwards with T <= this use the decode path
 constexpr int kMaxTopK = 8;
+constexpr int kGroupChunk = 2048;  // prefill grouping: slots per bucket-pass block
 constexpr int kWarps = 16;           // warps per CTA of the decode expert kernel
 
 struct MatLayout {
@@ -114,6 +115,7 @@ struct Plan {
   float* xsum = nullptr;        // [decode T][H / G] scale-group sums of the layer input
   uint16_t* pf_h = nullptr;     // prefill: [maxT * k][I] bf16 h per (expert, token) slot, perm order
   uint16_t* pf_o = nullptr;     // prefill: [maxT * k][H] bf16 weighted expert output per slot
+  int32_t* pf_bucket = nullptr;  // prefill grouping: [E][chunks of kGroupChunk slots] counts, then bases
   uint16_t* x_stage = nullptr;  // [maxT][H] for the host-buffer forward
   uint16_t* y_stage = nullptr;
 

@@ -341,7 +341,7 @@ void release(Plan* p) {
   for (auto* b : p->bias) cudaFree(b);
   void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
-                 p->wl_blob, p->ctl, p->hbuf, p->hsum, p->obuf, p->pf_h, p->pf_o, p->xsum, p->x_stage,
+                 p->wl_blob, p->ctl, p->hbuf, p->hsum, p->obuf, p->pf_h, p->pf_o, p->pf_bucket, p->xsum, p->x_stage,
                  p->y_stage, p->slot_of, p->slot_owner, p->lfu_count, p->lfu_last, p->miss_list,
                  p->miss_count, p->adm_list, p->adm_count, p->stats};
   for (void* v : dev)
@@ -475,6 +475,7 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   if (maxT > kDecodeMaxTokens) {
     ALLOC(p->pf_h, maxT * k * I);
     ALLOC(p->pf_o, maxT * k * H);
+    ALLOC(p->pf_bucket, E * ((maxT * k + kGroupChunk - 1) / kGroupChunk));
   }
   ALLOC(p->x_stage, maxT * H);
   ALLOC(p->y_stage, maxT * H);

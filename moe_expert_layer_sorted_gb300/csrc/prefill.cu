@@ -5,15 +5,17 @@
 //
 //   1. pf_router_kernel   fp32 router logits in the library's fixed summation
 //                         order (lane j of a warp owns elements 256m + 8j + r;
-//                         xor-butterfly; bias last), tiled 16 tokens x 16
-//                         experts per CTA, operands staged as fp32.
+//                         xor-butterfly; bias last), tiled 32 tokens x 16
+//                         experts per CTA (8 x 8 per warp), operands staged
+//                         as bf16 with cp.async, two buffers.
 //   2. pf_topk_kernel     per token: k largest logits (ties -> lower expert
 //                         index), softmax renormalised over the k.
-//   3. pf_count_kernel / pf_scan_kernel / pf_place_kernel
-//                         grouping by expert: per-expert counts, exclusive
-//                         offsets, and the stable (expert, token) order perm /
-//                         inv, one CTA per expert compacting the slots in
-//                         ascending order.
+//   3. pf_bucket_count / pf_bucket_scan / pf_bucket_place
+//                         grouping by expert: a stable counting sort of the
+//                         slots (per-block expert histograms, one prefix over
+//                         (expert, block), placement in slot order) giving
+//                         per-expert counts, offsets and the (expert, token)
+//                         order perm / inv.
 //   4. pf_gather_kernel   the layer input's rows copied into grouped
 //                         (expert, token) order.
 //   5. pf_gemm_kernel<gate/up>  for every routed (expert, 128 of its tokens,
@@ -59,63 +61,81 @@ namespace {
 
 // ------------------------------------------------------------------ router
 
-constexpr int kRtTile = 16;  // tokens and experts per router CTA
+constexpr int kRtTok = 32, kRtExp = 16;  // tokens and experts per router CTA (8 warps of 8 x 8)
 
-// xs/ws element (j, r) of a 256-wide block is stored at float4 index (r/4)*32 + j
-// so that the lanes' 16-byte reads are conflict-free.
+// Operands staged as bf16: row r of a 256-column block m holds, at uint4
+// index j, the elements 256m + 8j .. 256m + 8j + 7 (lane j's share in the
+// fixed order), so a lane's 16-byte reads are conflict-free.  Two buffers,
+// the next block's rows requested (cp.async) while the current one is used.
 __global__ void __launch_bounds__(256) pf_router_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                         const uint16_t* __restrict__ wr,
                                                         const float* __restrict__ bias, int E,
                                                         float* __restrict__ logits) {
-  __shared__ float4 xs[kRtTile][64];
-  __shared__ float4 ws[kRtTile][64];
+  __shared__ uint4 xs[2][kRtTok][32];
+  __shared__ uint4 ws[2][kRtExp][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t0 = blockIdx.x * kRtTile, e0 = blockIdx.y * kRtTile;
-  const int tw = (warp & 3) * 4, ew = (warp >> 2) * 8;  // warp tile: 4 tokens x 8 experts
-  float acc[4][8];
+  const int t0 = blockIdx.x * kRtTok, e0 = blockIdx.y * kRtExp;
+  const int tw = (warp & 3) * 8, ew = (warp >> 2) * 8;  // warp tile: 8 tokens x 8 experts
+  const int nm = H / 256;
+  // 48 rows x 32 pieces of 16 bytes per block, 6 per thread; rows past T or E read as zero
+  auto stage = [&](int m, int buf) {
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+    for (int i = 0; i < 6; ++i) {
+      const int c = tid + i * 256, row = c >> 5, j = c & 31;
+      const bool isx = row < kRtTok;
+      const int r = isx ? row : row - kRtTok;
+      const int g = isx ? t0 + r : e0 + r;
+      uint4* dst = isx ? &xs[buf][r][j] : &ws[buf][r][j];
+      if (g < (isx ? T : E)) cp_async16(dst, (isx ? x : wr) + (int64_t)g * H + m * 256 + j * 8);
+      else *dst = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
 #pragma unroll
     for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
-  for (int m = 0; m < H / 256; ++m) {
-    // stage: 16 rows x 32 uint4 of each operand; item i -> (operand, row, chunk j)
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int op = h >> 1, i = tid + (h & 1) * 256;  // i in 0..511
-      const int row = i >> 5, j = i & 31;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      const uint16_t* src = op == 0 ? x : wr;
-      const int lim = op == 0 ? T : E;
-      const int r0 = (op == 0 ? t0 : e0) + row;
-      if (r0 < lim) v = *reinterpret_cast<const uint4*>(src + (int64_t)r0 * H + m * 256 + j * 8);
-      float4* dst = op == 0 ? xs[row] : ws[row];
-      dst[j] = make_float4(bf16f(v.x & 0xffffu), bf16f(v.x >> 16), bf16f(v.y & 0xffffu), bf16f(v.y >> 16));
-      dst[32 + j] = make_float4(bf16f(v.z & 0xffffu), bf16f(v.z >> 16), bf16f(v.w & 0xffffu), bf16f(v.w >> 16));
+  stage(0, 0);
+  for (int m = 0; m < nm; ++m) {
+    const int buf = m & 1;
+    if (m + 1 < nm) {
+      stage(m + 1, buf ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    float xv[4][8], wv[8][8];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const float4 p = xs[tw + a][lane], q = xs[tw + a][32 + lane];
-      xv[a][0] = p.x; xv[a][1] = p.y; xv[a][2] = p.z; xv[a][3] = p.w;
-      xv[a][4] = q.x; xv[a][5] = q.y; xv[a][6] = q.z; xv[a][7] = q.w;
+    for (int h = 0; h < 2; ++h) {  // elements 4h .. 4h+3 of the lane's eight
+      uint2 xv[8], wv[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) xv[a] = reinterpret_cast<const uint2*>(&xs[buf][tw + a][lane])[h];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) wv[b] = reinterpret_cast<const uint2*>(&ws[buf][ew + b][lane])[h];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float xf[8], wf[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+          const uint32_t u = (r < 2) ? xv[a].x : xv[a].y;
+          xf[a] = (r & 1) ? __uint_as_float(u & 0xffff0000u) : bf16f(u & 0xffffu);
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const uint32_t u = (r < 2) ? wv[b].x : wv[b].y;
+          wf[b] = (r & 1) ? __uint_as_float(u & 0xffff0000u) : bf16f(u & 0xffffu);
+        }
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+          for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xf[a], wf[b], acc[a][b]);
+      }
     }
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const float4 p = ws[ew + b][lane], q = ws[ew + b][32 + lane];
-      wv[b][0] = p.x; wv[b][1] = p.y; wv[b][2] = p.z; wv[b][3] = p.w;
-      wv[b][4] = q.x; wv[b][5] = q.y; wv[b][6] = q.z; wv[b][7] = q.w;
-    }
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv[a][r], wv[b][r], acc[a][b]);
-    __syncthreads();
+    __syncthreads();  // the buffer is refilled two blocks later
   }
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < 8; ++a)
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       float v = acc[a][b];
@@ -173,66 +193,106 @@ __global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, i
 }
 
 // ------------------------------------------------------------------ grouping
+// A stable counting sort of the n = T*k slots by expert, in blocks of
+// kGroupChunk consecutive slots:
+//   pf_bucket_count  per block, the number of its slots routed to each expert;
+//   pf_bucket_scan   exclusive prefix over (expert, block), expert-major: the
+//                    first perm position of block b's slots of expert e; the
+//                    per-expert counts and offsets;
+//   pf_bucket_place  per block, warp w takes slots 256w..256w+255 of the block
+//                    in 32-slot rounds; a slot's position = its block's base
+//                    for its expert + the earlier warps' count + the slots of
+//                    its expert before it in its warp (match_any / popc).
+// Every slot lands in ascending (expert, slot) order: the order the oracle's
+// stable grouping defines.
 
-// Block-wide exclusive prefix of a 0/1 flag over blockDim.x (multiple of 32)
-// threads; returns the prefix and the block total in *tot.
-__device__ int block_prefix(int flag, int* wsum, int* tot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const unsigned b = __ballot_sync(0xffffffffu, flag);
-  const int inwarp = __popc(b & ((1u << lane) - 1u));
-  if (lane == 0) wsum[warp] = __popc(b);
+__global__ void __launch_bounds__(256) pf_bucket_count(const int32_t* __restrict__ idx, int n, int E,
+                                                       int32_t* __restrict__ bucket) {
+  extern __shared__ int32_t hist[];  // [E]
+  const int nb = gridDim.x, b = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  int before = 0, all = 0;
-  for (int w = 0; w < nw; ++w) {
-    const int c = wsum[w];
-    before += w < warp ? c : 0;
-    all += c;
+  const int s0 = b * kGroupChunk, s1 = min(n, s0 + kGroupChunk);
+  for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) atomicAdd(&hist[idx[s]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) bucket[(int64_t)e * nb + b] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024) pf_bucket_scan(int32_t* __restrict__ bucket, int E, int nb,
+                                                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int32_t part[1024];
+  const int tid = threadIdx.x;
+  const int64_t len = (int64_t)E * nb;
+  const int64_t per = (len + 1023) / 1024;
+  const int64_t i0 = tid * per, i1 = min(len, i0 + per);
+  int32_t sum = 0;
+  for (int64_t i = i0; i < i1; ++i) sum += bucket[i];
+  part[tid] = sum;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan of the 1024 partial sums
+    const int32_t v = tid >= o ? part[tid - o] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int32_t run = tid ? part[tid - 1] : 0;
+  for (int64_t i = i0; i < i1; ++i) {  // counts -> exclusive bases
+    const int32_t c = bucket[i];
+    bucket[i] = run;
+    run += c;
   }
   __syncthreads();
-  *tot = all;
-  return before + inwarp;
-}
-
-__global__ void pf_count_kernel(const int32_t* __restrict__ idx, int n, int32_t* __restrict__ counts) {
-  __shared__ int wsum[32];
-  const int e = blockIdx.x;
-  int total = 0;
-  for (int s0 = 0; s0 < n; s0 += blockDim.x) {
-    const int s = s0 + threadIdx.x;
-    int tot;
-    block_prefix(s < n && idx[s] == e, wsum, &tot);
-    total += tot;
+  for (int e = tid; e < E; e += 1024) {
+    const int32_t first = bucket[(int64_t)e * nb];
+    const int32_t next = e + 1 < E ? bucket[(int64_t)(e + 1) * nb] : part[1023];
+    offsets[e] = first;
+    counts[e] = next - first;
   }
-  if (threadIdx.x == 0) counts[e] = total;
+  if (tid == 0) offsets[E] = part[1023];
 }
 
-__global__ void pf_scan_kernel(const int32_t* __restrict__ counts, int E, int32_t* __restrict__ offsets) {
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int e = 0; e < E; ++e) {
-      offsets[e] = run;
-      run += counts[e];
-    }
-    offsets[E] = run;
+__global__ void __launch_bounds__(256) pf_bucket_place(const int32_t* __restrict__ idx, int n, int E,
+                                                       const int32_t* __restrict__ bucket,
+                                                       int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ int32_t wcnt[];  // [8 warps][E]
+  const int nb = gridDim.x, b = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int w0 = b * kGroupChunk + warp * (kGroupChunk / 8);
+  const int w1 = min(n, w0 + kGroupChunk / 8);
+  int32_t* mine = wcnt + warp * E;
+  for (int s0 = w0; s0 < w1; s0 += 32) {  // this warp's count per expert
+    const int s = s0 + lane;
+    const int e = s < w1 ? idx[s] : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (m & lt) == 0) mine[e] += __popc(m);
+    __syncwarp();
   }
-}
-
-// perm[offsets[e] + r] = the r-th slot (ascending) routed to e; inv is its inverse
-__global__ void pf_place_kernel(const int32_t* __restrict__ idx, int n, const int32_t* __restrict__ offsets,
-                                int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-  __shared__ int wsum[32];
-  const int e = blockIdx.x;
-  int base = offsets[e];
-  for (int s0 = 0; s0 < n; s0 += blockDim.x) {
-    const int s = s0 + threadIdx.x;
-    const bool f = s < n && idx[s] == e;
-    int tot;
-    const int r = block_prefix(f, wsum, &tot);
-    if (f) {
-      perm[base + r] = s;
-      inv[s] = base + r;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {  // -> each warp's first position per expert
+    int32_t run = bucket[(int64_t)e * nb + b];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int32_t c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
     }
-    base += tot;
+  }
+  __syncthreads();
+  for (int s0 = w0; s0 < w1; s0 += 32) {
+    const int s = s0 + lane;
+    const int e = s < w1 ? idx[s] : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int pos = mine[e] + __popc(m & lt);
+      perm[pos] = s;
+      inv[s] = pos;
+    }
+    __syncwarp();
+    if (e >= 0 && (m & lt) == 0) mine[e] += __popc(m);
+    __syncwarp();
   }
 }
 
@@ -735,21 +795,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
   }
 }
 
-// y[t][c] = sum over j ascending of o[inv[t*k + j]][c] (bf16 slot outputs, fp32 sum)
+// y[t][c] = sum over j ascending of o[inv[t*k + j]][c] (bf16 slot outputs, fp32 sum);
+// 8 columns per thread, the k slot rows' 16-byte pieces all requested before the sum
 __global__ void pf_combine_kernel(const uint16_t* __restrict__ o, const int32_t* __restrict__ inv, int T,
                                   int H, int k, uint16_t* __restrict__ y) {
-  const int64_t n = (int64_t)T * (H / 2);
+  const int per = H / 8;
+  const int64_t n = (int64_t)T * per;
+  const bool y16 = (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / (H / 2)), c = (int)(i % (H / 2)) * 2;
-    float s0 = 0.f, s1 = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(o + (int64_t)inv[(int64_t)t * k + j] * H + c);
-      s0 += bf16f(v & 0xffffu);
-      s1 += bf16f(v >> 16);
+    const int t = (int)(i / per), c = (int)(i % per);
+    uint4 v[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) v[j] = reinterpret_cast<const uint4*>(o)[(int64_t)inv[(int64_t)t * k + j] * per + c];
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          sum[2 * q] += bf16f(w[q] & 0xffffu);
+          sum[2 * q + 1] += bf16f(w[q] >> 16);
+        }
+      }
     }
-    *reinterpret_cast<uint32_t*>(y + (int64_t)t * H + c) =
-        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0)) |
-        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s1)) << 16);
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      out[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(sum[2 * q])) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(sum[2 * q + 1])) << 16);
+    if (y16) {
+      reinterpret_cast<uint4*>(y)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    } else {  // y need only be 4-byte aligned
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reinterpret_cast<uint32_t*>(y)[4 * i + q] = out[q];
+    }
   }
 }
 
@@ -871,13 +952,20 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   const int n = T * k;
   cudaError_t e;
   {
-    const dim3 grid((T + kRtTile - 1) / kRtTile, (E + kRtTile - 1) / kRtTile);
+    const dim3 grid((T + kRtTok - 1) / kRtTok, (E + kRtExp - 1) / kRtExp);
     pf_router_kernel<<<grid, 256, 0, s>>>(x, T, H, p.wr[layer], p.bias[layer], E, p.logits);
   }
   pf_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(p.logits, T, E, k, p.topk_idx, p.topk_w);
-  pf_count_kernel<<<E, 1024, 0, s>>>(p.topk_idx, n, p.counts);
-  pf_scan_kernel<<<1, 32, 0, s>>>(p.counts, E, p.offsets);
-  pf_place_kernel<<<E, 1024, 0, s>>>(p.topk_idx, n, p.offsets, p.perm, p.inv);
+  {
+    const int nb = (n + kGroupChunk - 1) / kGroupChunk;
+    const size_t hsm = (size_t)E * 4, wsm = (size_t)8 * E * 4;
+    if (wsm > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(pf_bucket_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm)) != cudaSuccess)
+      return e;
+    pf_bucket_count<<<nb, 256, hsm, s>>>(p.topk_idx, n, E, p.pf_bucket);
+    pf_bucket_scan<<<1, 1024, 0, s>>>(p.pf_bucket, E, nb, p.counts, p.offsets);
+    pf_bucket_place<<<nb, 256, wsm, s>>>(p.topk_idx, n, E, p.pf_bucket, p.perm, p.inv);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // token rows in grouped order, into the o buffer (free until the down projection)

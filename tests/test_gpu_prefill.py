@@ -111,3 +111,22 @@ def test_prefill_full_size_sampled():
                                       wl.scale_dtype, x[tok], wr, bias, np.arange(len(tok)))
     assert _rel_err(y[tok], ref) <= TOL
     plan.close()
+
+
+def test_prefill_output_4byte_aligned():
+    """The layer output may start on any 4-byte boundary (the ABI's rule for
+    y): a y offset by 4 bytes from a 16-byte boundary gets the same bits."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    wl, T = MID, 300
+    plan, info = harness.build_plan(wl, max_tokens=T)
+    x = torch.from_numpy(W.tokens(wl, 11, 0, T).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    plan.forward(0, x, y)
+    buf = torch.empty(T * wl.hidden + 8, dtype=torch.bfloat16, device="cuda")
+    y2 = buf[2:2 + T * wl.hidden].view(T, wl.hidden)
+    assert y2.data_ptr() % 16 == 4
+    plan.forward(0, x, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    plan.close()
