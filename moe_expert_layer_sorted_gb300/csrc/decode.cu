@@ -15,9 +15,10 @@
 //      - then runs its share of the work:
 //          A task (expert d, 16 rows of I): gate and up projections of those
 //            rows for the expert's tokens, streamed as NP units (column
-//            ranges of both matrices); at the end h = silu(g) * u in bf16,
+//            ranges of both matrices, up to 4096 columns per unit); at the
+//            end h = silu(g) * u in bf16,
 //            published to the other CTAs with the sums of each 16 h values;
-//          B unit (expert d, 64 rows of H): o = Wd h for those rows times the
+//          B unit (expert d, 128 rows of H): o = Wd h for those rows times the
 //            routing weight -> obuf[slot]; the B unit of the last distinct
 //            expert of a row block then sums each token's k slots (j
 //            ascending) into y (bf16).
@@ -675,8 +676,9 @@ expert_decode_kernel(ExpertArgs a) {
   // ---- work
   const uint32_t epoch = *reinterpret_cast<const volatile unsigned*>(a.epoch);
   const int tilesI = I / kTileRows;
-  const int nB = H / kBRows;                      // 64-row blocks of the down projection
-  const int NP = (nkbH + 7) / 8;                  // units per A task
+  const int nB = H / kBRows;                      // 128-row blocks of the down projection
+  const int NP = (nkbH + 15) / 16;                // units per A task (up to 16 column blocks of both
+                                                  // matrices per unit: two per warp)
   const int kbpp = (nkbH + NP - 1) / NP;          // column blocks per A unit (the last may have fewer)
   const int64_t b_codes = (int64_t)kBRows * KP * B / 8;
   const int b_scales = (kBRows / kTileRows) * ngI * kTileRows * ssz;
@@ -853,8 +855,8 @@ expert_decode_kernel(ExpertArgs a) {
     // A (task d, tile r, part pa): warp w takes matrix w&1 (gate / up) and
     //   the part's column blocks w>>1, w>>1 + 8, ...; B column g = token of
     //   the expert's slot g, against the layer input.
-    // B (expert d, row block r): warp w takes row tile w&3 and column blocks
-    //   w>>2, w>>2 + 4, ...; B column g = the expert's slot g, against h.
+    // B (expert d, row block r): warp w takes row tile w&7 and column blocks
+    //   w>>3, w>>3 + 2, ...; B column g = the expert's slot g, against h.
     // Columns g >= Te read a real row; their C columns are never used.
     const uint8_t* slot = ring + (size_t)sl * a.slot_bytes;
     const uint8_t* tbase;  // codes of the warp's tile, column block 0 of the unit
@@ -873,11 +875,11 @@ expert_decode_kernel(ExpertArgs a) {
       zb = csa;
       if (pa == 0) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     } else {
-      const int tl = warp & 3;
+      const int tl = warp & 7;  // row tile w % 8 of the unit's eight
       tbase = slot + (size_t)tl * nkbI * B * 512;
       scb = slot + b_codes;
       si = tl * ngI * kTileRows + g;
-      j0 = warp >> 2, jstep = kWarps / 4, jn = nkbI, kbase = 0;
+      j0 = warp >> 3, jstep = kWarps / 8, jn = nkbI, kbase = 0;
       bbase = hs + (size_t)(g < Te ? g : 0) * hrow + tig * 144;
       zb = csb;
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -945,10 +947,10 @@ expert_decode_kernel(ExpertArgs a) {
       for (int i2 = tid; i2 < kBRows * 8; i2 += kWarps * 32) {
         const int row = i2 >> 3, col = i2 & 7;
         if (col < Te) {
-          const int t4 = row >> 4, r16 = row & 15;
+          const int t4 = row >> 4, r16 = row & 15;  // row tile t4 of the unit's eight
           float o = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < kWarps / 4; ++ww) o += rb2[(4 * ww + t4) * 128 + r16 * 8 + col];
+          for (int ww = 0; ww < kWarps / 8; ++ww) o += rb2[(8 * ww + t4) * 128 + r16 * 8 + col];
           const int sl2 = R.perm[poff + col];
           st_relaxed_u64(a.obuf + (int64_t)sl2 * H + rb * kBRows + row,
                          tagged(__float_as_uint(R.w[sl2] * o), epoch));
@@ -1019,7 +1021,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   cudaError_t e = cudaSuccess;
   if (!cf.ready) {  // launch configuration for this batch size, once per plan
     const int KP = p.lay.m[2].kpad, ssz = scale_size(d.scale_dtype), b = d.weight_bits;
-    const int nkbH = H / kBlockK, NP = (nkbH + 7) / 8, kbpp = (nkbH + NP - 1) / NP;
+    const int nkbH = H / kBlockK, NP = (nkbH + 15) / 16, kbpp = (nkbH + NP - 1) / NP;
     const size_t a_unit = (size_t)2 * kbpp * b * 512 + (size_t)2 * kbpp * (kBlockK / G) * kTileRows * ssz;
     const size_t b_unit =
         (size_t)kBRows * KP * b / 8 + (size_t)(kBRows / kTileRows) * (KP / G) * kTileRows * ssz;

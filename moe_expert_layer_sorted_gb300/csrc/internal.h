@@ -31,7 +31,7 @@ namespace moe {
 // group g (ngroups counts the padded K).
 constexpr int kTileRows = 16;
 constexpr int kBlockK = 256;
-constexpr int kBRows = 64;           // rows of the down projection per B work unit
+constexpr int kBRows = 128;          // rows of the down projection per B work unit (8 row tiles)
 constexpr int kDecodeMaxTokens = 8;  // forwards with T <= this use the decode path
 constexpr int kMaxTopK = 8;
 constexpr int kGroupChunk = 2048;  // prefill grouping: slots per bucket-pass block
