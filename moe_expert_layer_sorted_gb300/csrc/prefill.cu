@@ -7,7 +7,7 @@
 //                         order (lane j of a warp owns elements 256m + 8j + r;
 //                         xor-butterfly; bias last), tiled 32 tokens x 16
 //                         experts per CTA (8 x 8 per warp), operands staged
-//                         as bf16 with cp.async, two buffers.
+//                         as bf16 with cp.async in a four-block ring.
 //   2. pf_topk_kernel     per token: k largest logits (ties -> lower expert
 //                         index), softmax renormalised over the k.
 //   3. pf_bucket_count / pf_bucket_scan / pf_bucket_place
@@ -62,57 +62,61 @@ namespace {
 // ------------------------------------------------------------------ router
 
 constexpr int kRtTok = 32, kRtExp = 16;  // tokens and experts per router CTA (8 warps of 8 x 8)
+constexpr int kRtStages = 4;             // 256-column blocks in flight (cp.async ring)
+constexpr size_t kRtStageBytes = (size_t)(kRtTok + kRtExp) * 32 * 16;
+constexpr size_t kRtSmem = kRtStages * kRtStageBytes;
 
 // Operands staged as bf16: row r of a 256-column block m holds, at uint4
 // index j, the elements 256m + 8j .. 256m + 8j + 7 (lane j's share in the
-// fixed order), so a lane's 16-byte reads are conflict-free.  Two buffers,
-// the next block's rows requested (cp.async) while the current one is used.
+// fixed order), so a lane's 16-byte reads are conflict-free.  A ring of
+// kRtStages blocks: block m + kRtStages - 1 is requested (cp.async) while
+// block m is used; one barrier per block.
 __global__ void __launch_bounds__(256) pf_router_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                         const uint16_t* __restrict__ wr,
                                                         const float* __restrict__ bias, int E,
                                                         float* __restrict__ logits) {
-  __shared__ uint4 xs[2][kRtTok][32];
-  __shared__ uint4 ws[2][kRtExp][32];
+  extern __shared__ __align__(16) uint4 rsm[];  // [stage][kRtTok + kRtExp rows][32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * kRtTok, e0 = blockIdx.y * kRtExp;
   const int tw = (warp & 3) * 8, ew = (warp >> 2) * 8;  // warp tile: 8 tokens x 8 experts
   const int nm = H / 256;
   // 48 rows x 32 pieces of 16 bytes per block, 6 per thread; rows past T or E read as zero
-  auto stage = [&](int m, int buf) {
+  auto stage = [&](int m) {
+    uint4* buf = rsm + (size_t)(m % kRtStages) * (kRtTok + kRtExp) * 32;
 #pragma unroll
     for (int i = 0; i < 6; ++i) {
       const int c = tid + i * 256, row = c >> 5, j = c & 31;
       const bool isx = row < kRtTok;
-      const int r = isx ? row : row - kRtTok;
-      const int g = isx ? t0 + r : e0 + r;
-      uint4* dst = isx ? &xs[buf][r][j] : &ws[buf][r][j];
+      const int g = isx ? t0 + row : e0 + row - kRtTok;
+      uint4* dst = buf + row * 32 + j;
       if (g < (isx ? T : E)) cp_async16(dst, (isx ? x : wr) + (int64_t)g * H + m * 256 + j * 8);
       else *dst = make_uint4(0, 0, 0, 0);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   };
   float acc[8][8];
 #pragma unroll
   for (int a = 0; a < 8; ++a)
 #pragma unroll
     for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
-  stage(0, 0);
+#pragma unroll
+  for (int m = 0; m < kRtStages - 1; ++m) {  // one commit group per block (empty past the end)
+    if (m < nm) stage(m);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   for (int m = 0; m < nm; ++m) {
-    const int buf = m & 1;
-    if (m + 1 < nm) {
-      stage(m + 1, buf ^ 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();
+    asm volatile("cp.async.wait_group %0;" ::"n"(kRtStages - 2) : "memory");  // block m has landed
+    __syncthreads();  // ... for every thread, and block m - 1's buffer is free
+    if (m + kRtStages - 1 < nm) stage(m + kRtStages - 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const uint4* xs = rsm + (size_t)(m % kRtStages) * (kRtTok + kRtExp) * 32;
+    const uint4* ws = xs + kRtTok * 32;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {  // elements 4h .. 4h+3 of the lane's eight
       uint2 xv[8], wv[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) xv[a] = reinterpret_cast<const uint2*>(&xs[buf][tw + a][lane])[h];
+      for (int a = 0; a < 8; ++a) xv[a] = reinterpret_cast<const uint2*>(&xs[(tw + a) * 32 + lane])[h];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) wv[b] = reinterpret_cast<const uint2*>(&ws[buf][ew + b][lane])[h];
+      for (int b = 0; b < 8; ++b) wv[b] = reinterpret_cast<const uint2*>(&ws[(ew + b) * 32 + lane])[h];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         float xf[8], wf[8];
@@ -132,8 +136,8 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const uint16_t* __restri
           for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xf[a], wf[b], acc[a][b]);
       }
     }
-    __syncthreads();  // the buffer is refilled two blocks later
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
   for (int a = 0; a < 8; ++a)
 #pragma unroll
@@ -953,7 +957,10 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   cudaError_t e;
   {
     const dim3 grid((T + kRtTok - 1) / kRtTok, (E + kRtExp - 1) / kRtExp);
-    pf_router_kernel<<<grid, 256, 0, s>>>(x, T, H, p.wr[layer], p.bias[layer], E, p.logits);
+    if ((e = cudaFuncSetAttribute(pf_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem)) !=
+        cudaSuccess)
+      return e;
+    pf_router_kernel<<<grid, 256, kRtSmem, s>>>(x, T, H, p.wr[layer], p.bias[layer], E, p.logits);
   }
   pf_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(p.logits, T, E, k, p.topk_idx, p.topk_w);
   {
