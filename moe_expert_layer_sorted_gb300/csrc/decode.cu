@@ -17,7 +17,7 @@
 //            rows for the expert's tokens, streamed as NP units (column
 //            ranges of both matrices, up to 4096 columns per unit); at the
 //            end h = silu(g) * u in bf16,
-//            published to the other CTAs with the sums of each 16 h values;
+//            published to the other CTAs;
 //          B unit (expert d, 128 rows of H): o = Wd h for those rows times the
 //            routing weight -> obuf[slot]; the B unit of the last distinct
 //            expert of a row block then sums each token's k slots (j
@@ -220,7 +220,6 @@ struct ExpertArgs {
   int miss_cap;
   const unsigned* epoch;
   unsigned long long* hbuf;  // [maxD][tstride][kpadI/2] tagged bf16 pairs of h
-  unsigned long long* hsum;  // [maxD][tstride][kpadI/16] tagged fp32 sums of 16 h values
   unsigned long long* obuf;  // [T*k][H] tagged fp32 weighted expert outputs
   int tstride;
   uint16_t* y;
@@ -387,10 +386,7 @@ expert_decode_kernel(ExpertArgs a) {
   off += ((size_t)ngI * 9 * 4 + 15) / 16 * 16;
   float* red = reinterpret_cast<float*>(sm + off);  // [2][kWarps][16][8] per-warp partials
   off += (size_t)2 * kWarps * 128 * 4;
-  float* gus = reinterpret_cast<float*>(sm + off);  // [2][16][8] gate, up of an A task
-  off += 2 * 128 * 4;
-  uint16_t* hq = reinterpret_cast<uint16_t*>(sm + off);  // [8][16] bf16 h of an A task
-  off += 128 * 2;
+
   uint8_t* ring = sm + off;  // a.nslots units
 
   for (int i = tid; i < ngH; i += blockDim.x) csa[i * 9 + 8] = 0.f;
@@ -833,17 +829,31 @@ expert_decode_kernel(ExpertArgs a) {
           }
         }
       }
+      consumer_sync();
+      // zero-point group sums of h: fp32 sums of 16 rows (ascending), then of a
+      // group's 16-row sums; scratch in the half of red the next reduction uses
+      // (the previous unit's readers use the other half)
+      float* ssum = red + (rp & 1) * kWarps * 128;  // [Te][tilesI]
+      for (int q = tid; q < Te * tilesI; q += kWarps * 32) {
+        const int n = q / tilesI, mt = q % tilesI;
+        const uint8_t* hrow_n = hs + (size_t)n * hrow;
+        float s16 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t pr = *reinterpret_cast<const uint32_t*>(hrow_n + frag_offset(2 * (8 * mt + c)));
+          s16 += bf16f(pr & 0xffffu);
+          s16 += bf16f(pr >> 16);
+        }
+        ssum[q] = s16;
+      }
+      consumer_sync();
       const int tpg = G / kTileRows;  // 16-row sums per scale group
-      const unsigned long long* ssrc = a.hsum + (int64_t)d * a.tstride * (KP / 16);
       for (int q = tid; q < ngI * Te; q += kWarps * 32) {
         const int grp = q % ngI, n = q / ngI;
         float sv = 0.f;
         for (int j = 0; j < tpg; ++j) {
           const int mt = grp * tpg + j;
-          if (mt < tilesI) {
-            const unsigned long long* pw = ssrc + n * (KP / 16) + mt;
-            sv += __uint_as_float(payload_of(pw, ld_relaxed_u64(pw), epoch, a.err));
-          }
+          if (mt < tilesI) sv += ssum[n * tilesI + mt];
         }
         csb[grp * 9 + n] = a.zcorr * sv;
       }
@@ -906,32 +916,20 @@ expert_decode_kernel(ExpertArgs a) {
         rw[(g + 8) * 8 + c0] = acc[2];
         rw[(g + 8) * 8 + c1] = acc[3];
         consumer_sync();
-        if (tid < 256) {
-          const int m2 = tid >> 7, e = tid & 127;
-          float v = 0.f;
-#pragma unroll
-          for (int ww = 0; ww < kWarps / 2; ++ww) v += rb2[(2 * ww + m2) * 128 + e];
-          gus[tid] = v;
-        }
-        consumer_sync();
-        if (tid < 128) {
+        if (tid < 128) {  // (row, token slot) = (tid / 8, tid % 8): gate and up over the warps, h
           const int row = tid >> 3, col = tid & 7;
-          const float gv = gus[tid], uv = gus[128 + tid];
-          const float h = gv / (1.0f + expf(-gv)) * uv;
-          hq[col * 16 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
-        }
-        consumer_sync();
-        if (tid < 8 * Te) {  // bf16 pairs (rows 2q, 2q+1) of token slot n
-          const int n = tid >> 3, q = tid & 7;
-          const uint32_t pr = (uint32_t)hq[n * 16 + 2 * q] | ((uint32_t)hq[n * 16 + 2 * q + 1] << 16);
-          st_relaxed_u64(a.hbuf + ((int64_t)d * a.tstride + n) * (KP / 2) + mt * 8 + q, tagged(pr, epoch));
-        } else if (tid >= 256 && tid < 256 + Te) {  // sum of the 16 bf16 values, rows ascending
-          const int n = tid - 256;
-          float sv = 0.f;
+          float gv = 0.f, uv = 0.f;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) sv += bf16f(hq[n * 16 + q]);
-          st_relaxed_u64(a.hsum + ((int64_t)d * a.tstride + n) * (KP / 16) + mt,
-                         tagged(__float_as_uint(sv), epoch));
+          for (int ww = 0; ww < kWarps / 2; ++ww) {
+            gv += rb2[(2 * ww) * 128 + tid];
+            uv += rb2[(2 * ww + 1) * 128 + tid];
+          }
+          const float h = gv / (1.0f + expf(-gv)) * uv;
+          const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+          const uint32_t next = __shfl_down_sync(0xffffffffu, hb, 8);  // row + 1, same token slot
+          if (!(row & 1) && col < Te)  // bf16 pair (rows row, row + 1) of token slot col
+            st_relaxed_u64(a.hbuf + ((int64_t)d * a.tstride + col) * (KP / 2) + mt * 8 + (row >> 1),
+                           tagged(hb | (next << 16), epoch));
         }
       }
     } else {
@@ -1029,7 +1027,7 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
     const size_t ngH = H / G, ngI = KP / G;
     const size_t fixed = (size_t)T * frag_row_bytes(H / kBlockK) + (ngH * 9 * 4 + 15) / 16 * 16 +
                          (size_t)T * frag_row_bytes(KP / kBlockK) + (ngI * 9 * 4 + 15) / 16 * 16 +
-                         (size_t)2 * kWarps * 128 * 4 + 2 * 128 * 4 + 128 * 2;
+                         (size_t)2 * kWarps * 128 * 4;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device);
     if (e != cudaSuccess) return e;
@@ -1098,7 +1096,6 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.miss_cap = d.num_layers * p.max_distinct;
   a.epoch = &p.ctl->epoch;
   a.hbuf = p.hbuf;
-  a.hsum = p.hsum;
   a.tstride = std::min(d.max_tokens, kDecodeMaxTokens);
   a.obuf = p.obuf;
   a.y = y;

@@ -110,7 +110,6 @@ struct Plan {
   // Hand-off words between CTAs of the decode expert kernel: 32-bit payload in
   // the low half, the forward's epoch in the high half (zeroed at creation).
   unsigned long long* hbuf = nullptr;  // [maxD][decode T][kpad(I)/2] bf16 pairs of h
-  unsigned long long* hsum = nullptr;  // [maxD][decode T][kpad(I)/16] fp32 sums of 16 h values
   unsigned long long* obuf = nullptr;  // [decode T * k][H] fp32 weighted expert outputs per slot
   float* xsum = nullptr;        // [decode T][H / G] scale-group sums of the layer input
   uint16_t* pf_h = nullptr;     // prefill: [maxT * k][I] bf16 h per (expert, token) slot, perm order

@@ -341,7 +341,7 @@ void release(Plan* p) {
   for (auto* b : p->bias) cudaFree(b);
   void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
-                 p->wl_blob, p->ctl, p->hbuf, p->hsum, p->obuf, p->pf_h, p->pf_o, p->pf_bucket, p->xsum, p->x_stage,
+                 p->wl_blob, p->ctl, p->hbuf, p->obuf, p->pf_h, p->pf_o, p->pf_bucket, p->xsum, p->x_stage,
                  p->y_stage, p->slot_of, p->slot_owner, p->lfu_count, p->lfu_last, p->miss_list,
                  p->miss_count, p->adm_list, p->adm_count, p->stats};
   for (void* v : dev)
@@ -469,7 +469,6 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   ALLOC(p->ctl, 1);
   const int64_t KPI = p->lay.m[2].kpad;
   ALLOC(p->hbuf, maxD * decT * (KPI / 2));
-  ALLOC(p->hsum, maxD * decT * (KPI / 16));
   ALLOC(p->obuf, decT * k * H);
   ALLOC(p->xsum, decT * (H / d.group_size));
   if (maxT > kDecodeMaxTokens) {
@@ -506,7 +505,6 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   cudaMemset(p->blob_host, 0, LE * sizeof(void*));
   cudaMemset(p->ctl, 0, sizeof(Ctl));
   cudaMemset(p->hbuf, 0, (size_t)maxD * decT * (KPI / 2) * 8);  // epoch 0: never current
-  cudaMemset(p->hsum, 0, (size_t)maxD * decT * (KPI / 16) * 8);
   cudaMemset(p->obuf, 0, (size_t)decT * k * H * 8);
   cudaMemset(p->stats, 0, (size_t)d.num_layers * kNumStats * 8);
   if (d.cache_policy == MOE_POLICY_LFU) {
