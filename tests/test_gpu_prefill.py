@@ -130,3 +130,38 @@ def test_prefill_output_4byte_aligned():
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
     plan.close()
+
+
+MIDH = W.Workload("prefill-mid-host", 1, 8, 512, 256, 2, (300,), 4, 64, W.SC_F32, "zipf", 1.0, host_total=4)
+MID3H = W.Workload("prefill-mid3-host", 1, 12, 512, 256, 3, (700,), 3, 128, W.SC_BF16, "zipf", 1.0,
+                   host_total=7)
+
+
+@pytest.mark.parametrize("wl,T", [(MIDH, 300), (MID3H, 700)])
+def test_prefill_host_resident(wl, T):
+    """Experts in pinned host memory are read in place by the prefill GEMMs
+    (16-byte cp.async of their code blocks instead of bulk copies): the layer
+    output is bit-identical to a plan with every expert in HBM, within
+    tolerance of the oracle, and the forward counts each routed host expert as
+    a miss."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    plan, info = harness.build_plan(wl, max_tokens=T)
+    ref_plan, _ = harness.build_plan(wl, max_tokens=T, all_hbm=True)
+    wr, bias, _ = info["routers"][0]
+    host = info["host_sets"][0]
+    assert len(host) == wl.host_total
+    x = W.tokens(wl, 3 + T, 0, T)
+    y, r = _run(plan, x, wl)
+    y_ref, _ = _run(ref_plan, x, wl)
+    assert np.array_equal(y, y_ref)
+    experts = [_oracle_expert(wl, 0, e) for e in range(wl.experts)]
+    ref = oracle.layer_forward(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                               wl.scale_dtype, x, wr, bias)
+    assert _rel_err(y, ref["y"]) <= TOL
+    routed = set(int(e) for e in np.nonzero(ref["counts"])[0])
+    assert routed & host, "the case must route tokens to host-resident experts"
+    st = plan.stats(0)
+    assert st["misses"] == len(routed & host) and st["hits"] == len(routed - host)
+    plan.close()
+    ref_plan.close()
