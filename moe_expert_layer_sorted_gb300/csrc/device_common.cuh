@@ -88,19 +88,40 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
   return d;
 }
 
+// (128 + c u) -> (128 + u) in both bf16 halves, c = 1/mul: exact (a power-of-two
+// scale and a sum that bf16 represents)
+__device__ __forceinline__ uint32_t rescale_bf16x2(uint32_t v, uint32_t mul2, uint32_t add2) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(v), "r"(mul2), "r"(add2));
+  return d;
+}
+
 // bf16x2 register (128 + u_lo, 128 + u_hi) of pair P (0..63) of a lane's
 // 256-column block held in w (its 4*B words); P is a compile-time constant
 // after unrolling.  Field placement: see repack_codes_kernel in plan.cu.
+// A field in bits 0..6 of a half-word can be masked straight into the bf16
+// mantissa of 128 (value 128 + 2^s u for a field at bit s), so only every
+// second or third field needs a shift; those at s > 0 are rescaled by one
+// bf16x2 fma (u < 2^b, so every intermediate is exact).
 template <int B>
 __device__ __forceinline__ uint32_t pair_of(const uint32_t (&w)[4 * B], int P) {
   constexpr uint32_t kMagic = 0x43004300u;  // bf16 128.0 in both halves
   if constexpr (B == 4) {
     return and_or(w[P >> 2] >> (4 * (P & 3)), 0x000F000Fu, kMagic);
-  } else if constexpr (B == 2) {
-    return and_or(w[P >> 3] >> (2 * (P & 7)), 0x00030003u, kMagic);
+  } else if constexpr (B == 2) {  // fields at bits 0, 2, 4 | 6, 8, 10 | 12, 14
+    const uint32_t x = w[P >> 3] >> (6 * ((P & 7) / 3));
+    switch ((P & 7) % 3) {
+      case 0: return and_or(x, 0x00030003u, kMagic);
+      case 1: return rescale_bf16x2(and_or(x, 0x000C000Cu, kMagic), 0x3E803E80u, 0x42C042C0u);  // 0.25, 96
+      default: return rescale_bf16x2(and_or(x, 0x00300030u, kMagic), 0x3D803D80u, 0x42F042F0u);  // 1/16, 120
+    }
   } else {
     const int t = P >> 4, m = P & 15;
-    if (m < 15) return and_or(w[3 * t + m / 5] >> (3 * (m % 5)), 0x00070007u, kMagic);
+    if (m < 15) {  // fields at bits 0, 3 | 6, 9 | 12
+      const uint32_t x = w[3 * t + m / 5] >> (6 * ((m % 5) / 2));
+      if ((m % 5) % 2 == 0) return and_or(x, 0x00070007u, kMagic);
+      return rescale_bf16x2(and_or(x, 0x00380038u, kMagic), 0x3E003E00u, 0x42E042E0u);  // 0.125, 112
+    }
     const uint32_t v = and_or(w[3 * t] >> 15, 0x00010001u, kMagic);
     const uint32_t u = and_or(w[3 * t + 1] >> 14, 0x00020002u, v);
     return and_or(w[3 * t + 2] >> 13, 0x00040004u, u);
