@@ -63,6 +63,27 @@ def _recorded_traffic(name: str):
         return None
 
 
+def _numa_node(device: int = 0):
+    """{"pci_bus_id", "numa_node"} of the GPU (NVML and sysfs); a field is None
+    where it cannot be read."""
+    out = {"pci_bus_id": None, "numa_node": None}
+    try:
+        import pynvml
+        pynvml.nvmlInit()
+        bus = pynvml.nvmlDeviceGetPciInfo(pynvml.nvmlDeviceGetHandleByIndex(device)).busId
+        bus = bus.decode() if isinstance(bus, bytes) else bus
+        out["pci_bus_id"] = bus
+        for cand in (bus.lower(), bus.lower()[-12:]):  # sysfs names use a 4-digit domain
+            path = f"/sys/bus/pci/devices/{cand}/numa_node"
+            if os.path.exists(path):
+                with open(path) as f:
+                    out["numa_node"] = int(f.read().strip())
+                break
+    except Exception:
+        pass
+    return out
+
+
 def _tensor_peak():
     """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed alone)."""
     try:
@@ -326,6 +347,7 @@ def run_ours(args):
     value = ws * tokens_step / (ms_step * 1e-3)
     achieved = (hbm_b + host_b) / (ms_step * 1e-3) / 1e9
     roof_s = hbm_b / (hbm_peak * 1e9) + host_b / (link_gbs * 1e9)
+    roof_max_s = max(hbm_b / (hbm_peak * 1e9), host_b / (link_gbs * 1e9))  # perfect link/HBM overlap
     eff_peak = (hbm_b + host_b) / roof_s / 1e9
 
     # per batch size (separate timing of each forward, same protocol)
@@ -347,9 +369,11 @@ def run_ours(args):
         s2 = plan.stats(0)
         hb, ob = s2["hbm_bytes"] / 16, s2["host_bytes"] / 16
         rt = hb / (hbm_peak * 1e9) + ob / (link_gbs * 1e9)
+        rtm = max(hb / (hbm_peak * 1e9), ob / (link_gbs * 1e9))
         per_batch[str(T)] = {"tokens_per_s": T / (m * 1e-3), "us_per_forward": m * 1e3,
                              "hbm_MB": hb / 1e6, "host_MB": ob / 1e6,
-                             "roofline_us": rt * 1e6, "roofline_frac": rt / (m * 1e-3)}
+                             "roofline_us": rt * 1e6, "roofline_frac": rt / (m * 1e-3),
+                             "roofline_frac_max_form": rtm / (m * 1e-3)}
 
     # end to end through the host-buffer entry point (pinned buffers, copies timed)
     xh = {T: [xs[T][s].view(torch.int16).cpu().pin_memory() for s in range(4)] for T in BATCHES}
@@ -396,9 +420,11 @@ def run_ours(args):
                          "peak_note": f"sum-form roofline: HBM {hbm_peak:.0f} GB/s ({peak_kind}, "
                                       f"MEASURED_PEAKS.json) for HBM bytes + measured host link "
                                       f"{link_gbs:.1f} GB/s for host bytes",
-                         "hbm_bytes_per_step": hbm_b, "host_bytes_per_step": host_b},
+                         "hbm_bytes_per_step": hbm_b, "host_bytes_per_step": host_b,
+                         "frac_max_form": roof_max_s / (ms_step * 1e-3)},
             "per_batch": per_batch,
-            "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe},
+            "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
+                     "gpu": _numa_node(local)},
             "e2e": {"value": ws * tokens_step / (e2e_step * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
             "gpu_launches": 2 * len(BATCHES) * args.steps,
@@ -491,9 +517,11 @@ def run_stack(args):
         stt = plan.stats(-1)
         hb, ob = stt["hbm_bytes"] / args.steps, stt["host_bytes"] / args.steps
         roof = hb / (hbm_peak * 1e9) + ob / (link_gbs * 1e9)
+        roof_max = max(hb / (hbm_peak * 1e9), ob / (link_gbs * 1e9))
         per_T[str(T)] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms, "hbm_GB_per_step": hb / 1e9,
                          "host_GB_per_step": ob / 1e9, "weight_stream_GBps": (hb + ob) / (ms * 1e-3) / 1e9,
-                         "roofline_ms": roof * 1e3, "roofline_frac": roof / (ms * 1e-3), "clocks": ck}
+                         "roofline_ms": roof * 1e3, "roofline_frac": roof / (ms * 1e-3),
+                         "roofline_frac_max_form": roof_max / (ms * 1e-3), "clocks": ck}
         launches = 2 * L * args.steps
         del graphs
     T_head = str(max(wl.tokens))
@@ -504,8 +532,10 @@ def run_stack(args):
          "l2": "no flush: one step streams ~1-4 GB of weights, far above L2", "cuda_graph": True,
          "parallelism": "single GPU"},
         {"per_T": per_T, "setup_s": build_s,
-         "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe},
+         "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
+                  "gpu": _numa_node(0)},
          "roofline": {"bound": "hbm", "frac": per_T[T_head]["roofline_frac"],
+                      "frac_max_form": per_T[T_head]["roofline_frac_max_form"],
                       "peak_note": f"sum form: HBM {hbm_peak:.0f} GB/s ({peak_kind}) + host link {link_gbs:.1f} GB/s"},
          "gpu_launches": launches, "clocks": per_T[T_head]["clocks"]})
     print(json.dumps(line), flush=True)
@@ -577,32 +607,42 @@ def run_cached(args):
     clocks.start()
     a = torch.cuda.Event(enable_timing=True)
     m = torch.cuda.Event(enable_timing=True)
+    m2 = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    st_half = None
     with torch.cuda.stream(stream):
         a.record(stream)
         for st in range(S):
-            if st == half:
+            if st == half:  # counters of the first half: read between the two timed halves
                 m.record(stream)
+                stream.synchronize()
+                st_half = plan.stats(-1)
+                m2.record(stream)
             stage(st)
             g.replay()
         b.record(stream)
     torch.cuda.synchronize()
     ck = clocks.stop()
-    total_ms = a.elapsed_time(b)
+    total_ms = a.elapsed_time(m) + m2.elapsed_time(b)
     st_all = plan.stats(-1)
     line = _common_line(
         args, "MoE decode tokens/s (cached 48-layer decode)", S / (total_ms * 1e-3), "tokens/s", total_ms / S,
         {"workload": wl.desc.replace("2048 steps", f"{S} steps"), "tokens_per_step": 1,
          "l2": "no flush: a step touches ~440 MB", "cuda_graph": True, "parallelism": "single GPU"},
         {"hit_rate": st_all["hits"] / max(st_all["accesses"], 1),
+         "hit_rate_second_half": (st_all["hits"] - st_half["hits"]) / max(st_all["accesses"] - st_half["accesses"], 1),
          "cache": {k: st_all[k] for k in ("accesses", "hits", "misses", "admissions", "evictions",
                                           "hbm_bytes", "host_bytes", "fill_bytes")},
          "weight_stream_GBps": (st_all["hbm_bytes"] + st_all["host_bytes"]) / (total_ms * 1e-3) / 1e9,
          "roofline": {"bound": "hbm", "frac": (st_all["hbm_bytes"] / (hbm_peak * 1e9) + st_all["host_bytes"] / (link_gbs * 1e9)
                                                + st_all["fill_bytes"] / (link_gbs * 1e9)) / (total_ms * 1e-3),
+                      "frac_max_form": max(st_all["hbm_bytes"] / (hbm_peak * 1e9),
+                                           (st_all["host_bytes"] + st_all["fill_bytes"]) / (link_gbs * 1e9)) / (total_ms * 1e-3),
                       "peak_note": f"sum form: HBM {hbm_peak:.0f} GB/s ({peak_kind}) + host link {link_gbs:.1f} GB/s "
                                    "(misses and cache fills both cross the link)"},
-         "second_half_ms_per_step": m.elapsed_time(b) / (S - half),
+         "second_half_ms_per_step": m2.elapsed_time(b) / (S - half),
+         "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
+                  "gpu": _numa_node(0)},
          "setup_s": build_s, "gpu_launches": (2 * L + 2) * S, "clocks": ck})
     print(json.dumps(line), flush=True)
     plan.close()
