@@ -68,11 +68,21 @@ def _numa_node(device: int = 0):
     where it cannot be read."""
     out = {"pci_bus_id": None, "numa_node": None}
     try:
-        import pynvml
-        pynvml.nvmlInit()
-        bus = pynvml.nvmlDeviceGetPciInfo(pynvml.nvmlDeviceGetHandleByIndex(device)).busId
-        bus = bus.decode() if isinstance(bus, bytes) else bus
-        out["pci_bus_id"] = bus
+        import torch
+        pr = torch.cuda.get_device_properties(device)
+        bus = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except Exception:
+        bus = None
+    if bus is None:
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            bus = pynvml.nvmlDeviceGetPciInfo(pynvml.nvmlDeviceGetHandleByIndex(device)).busId
+            bus = bus.decode() if isinstance(bus, bytes) else bus
+        except Exception:
+            return out
+    out["pci_bus_id"] = bus
+    try:
         for cand in (bus.lower(), bus.lower()[-12:]):  # sysfs names use a 4-digit domain
             path = f"/sys/bus/pci/devices/{cand}/numa_node"
             if os.path.exists(path):
