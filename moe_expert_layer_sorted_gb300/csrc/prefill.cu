@@ -161,7 +161,35 @@ __global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, i
   const float* l = logits + (int64_t)t * E;
   int chosen[kMaxTopK];
   float cv[kMaxTopK];
-  for (int j = 0; j < k; ++j) {
+  if (E <= 16 * 32) {  // the lane's logits (experts lane, lane + 32, ...) held in registers
+    float vb[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) vb[q] = q * 32 + lane < E ? l[q * 32 + lane] : 0.0f;
+    uint32_t taken = 0u;
+    for (int j = 0; j < k; ++j) {
+      uint32_t best = 0u;
+      float bv = 0.0f;
+      int bq = -1;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float v = vb[q];
+        const uint32_t ub = __float_as_uint(v == 0.0f ? 0.0f : v);
+        const uint32_t key = (ub & 0x80000000u) ? ~ub : (ub | 0x80000000u);
+        if (q * 32 + lane < E && !((taken >> q) & 1u) && (bq < 0 || key > best)) {  // ascending e: ties keep the lower
+          best = key;
+          bv = v;
+          bq = q;
+        }
+      }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bq < 0 ? 0u : best);
+      const uint32_t mine = (bq >= 0 && best == kmax) ? (uint32_t)(bq * 32 + lane) : 0xffffffffu;
+      const int win = (int)__reduce_min_sync(0xffffffffu, mine);
+      if (bq >= 0 && bq * 32 + lane == win) taken |= 1u << bq;
+      chosen[j] = win;
+      cv[j] = __shfl_sync(0xffffffffu, bv, win & 31);
+    }
+  }
+  for (int j = 0; j < k && E > 16 * 32; ++j) {
     uint32_t best = 0u;
     int bi = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
@@ -303,15 +331,30 @@ __global__ void __launch_bounds__(256) pf_bucket_place(const int32_t* __restrict
 // ------------------------------------------------------------------ token rows in (expert, token) order
 
 // xp[p] = x[perm[p] / k]: the layer input gathered into the grouped order, so
-// that every GEMM unit's token rows are one contiguous tile for the TMA.
-__global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int n, int k,
-                                 int H, uint16_t* __restrict__ xp) {
+// that every GEMM unit's token rows are one contiguous tile for the TMA.  One
+// warp per row: one perm lookup, then the row's 16-byte pieces, up to 16 per
+// lane in flight.
+__global__ void __launch_bounds__(256) pf_gather_kernel(const uint16_t* __restrict__ x,
+                                                        const int32_t* __restrict__ perm, int n, int k, int H,
+                                                        uint16_t* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
   const int per = H / 8;  // 16-byte pieces per row
-  const int64_t tot = (int64_t)n * per;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < tot; i += (int64_t)gridDim.x * blockDim.x) {
-    const int p = (int)(i / per), c = (int)(i % per);
-    const int t = perm[p] / k;
-    reinterpret_cast<uint4*>(xp)[i] = reinterpret_cast<const uint4*>(x)[(int64_t)t * per + c];
+  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n; p += gridDim.x * (blockDim.x >> 5)) {
+    const uint4* src = reinterpret_cast<const uint4*>(x) + (int64_t)(perm[p] / k) * per;
+    uint4* dst = reinterpret_cast<uint4*>(xp) + (int64_t)p * per;
+    for (int c0 = 0; c0 < per; c0 += 16 * 32) {
+      uint4 v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int c = c0 + q * 32 + lane;
+        if (c < per) v[q] = src[c];
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int c = c0 + q * 32 + lane;
+        if (c < per) dst[c] = v[q];
+      }
+    }
   }
 }
 
@@ -976,7 +1019,7 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // token rows in grouped order, into the o buffer (free until the down projection)
-  pf_gather_kernel<<<4 * p.sms, 256, 0, s>>>(x, p.perm, n, k, H, p.pf_o);
+  pf_gather_kernel<<<std::min((n + 7) / 8, 16 * p.sms), 256, 0, s>>>(x, p.perm, n, k, H, p.pf_o);
 
   const int64_t ge0 = (int64_t)layer * E;
   const int G = d.group_size;
