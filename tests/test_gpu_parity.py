@@ -209,3 +209,31 @@ def test_decode_layer_full_size(decode_layer, T):
             break
     st = plan.stats(0)
     assert st["accesses"] - st0["accesses"] == st["hits"] - st0["hits"] + st["misses"] - st0["misses"]
+
+
+# more experts than one warp's 16 registers per lane hold (the list-based top-k
+# of the decode prologue); T = 1, 5, 8
+WIDE = W.Workload("decode-wide", 1, 600, 256, 128, 5, (8,), 3, 64, W.SC_BF16, "zipf", 1.0, host_total=150)
+
+
+@pytest.mark.parametrize("T", [1, 5, 8])
+def test_wide_router_layer(T):
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = WIDE
+    plan, info = harness.build_plan(wl)
+    wr, bias, _ = info["routers"][0]
+    x = W.tokens(wl, 300 + T, 0, T)
+    y, r = _run(plan, 0, x, wl)
+    routed = np.unique(r["topk_idx"])
+    experts = [_oracle_expert(wl, 0, e) if e in routed else None for e in range(wl.experts)]
+    ref = oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                                      wl.scale_dtype, x, wr, bias, np.arange(T))
+    lg = oracle.router_logits(x, wr, bias)
+    idx, w = oracle.topk(lg, wl.top_k)
+    assert np.array_equal(r["logits"], lg)
+    assert np.array_equal(r["topk_idx"], idx)
+    np.testing.assert_allclose(r["topk_w"], w, rtol=2e-6, atol=1e-7)
+    counts, offsets, perm, inv = oracle.permute(idx, wl.experts)
+    assert np.array_equal(r["counts"], counts) and np.array_equal(r["perm"], perm)
+    assert _rel_err(_bf16_bits_to_f64(y), ref) <= TOL
+    plan.close()

@@ -165,3 +165,30 @@ def test_prefill_host_resident(wl, T):
     assert st["misses"] == len(routed & host) and st["hits"] == len(routed - host)
     plan.close()
     ref_plan.close()
+
+
+WIDEP = W.Workload("prefill-wide", 1, 600, 256, 128, 5, (40,), 4, 64, W.SC_F32, "zipf", 1.0)
+
+
+def test_prefill_wide_router():
+    """More experts than the register path of the prefill top-k holds (E > 512):
+    routing bit-exact, outputs of the layer within tolerance."""
+    from moe_expert_layer_sorted_gb300 import harness
+    wl, T = WIDEP, 40
+    plan, info = harness.build_plan(wl, max_tokens=T)
+    wr, bias, _ = info["routers"][0]
+    x = W.tokens(wl, 17, 0, T)
+    y, r = _run(plan, x, wl)
+    lg = oracle.router_logits(x, wr, bias)
+    idx, w = oracle.topk(lg, wl.top_k)
+    assert np.array_equal(r["logits"], lg)
+    assert np.array_equal(r["topk_idx"], idx)
+    np.testing.assert_allclose(r["topk_w"], w, rtol=2e-6, atol=1e-7)
+    counts, offsets, perm, inv = oracle.permute(idx, wl.experts)
+    assert np.array_equal(r["counts"], counts) and np.array_equal(r["offsets"], offsets)
+    assert np.array_equal(r["perm"], perm) and np.array_equal(r["inv"], inv)
+    experts = [_oracle_expert(wl, 0, e) if e in np.unique(idx) else None for e in range(wl.experts)]
+    ref = oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                                      wl.scale_dtype, x, wr, bias, np.arange(T))
+    assert _rel_err(y, ref) <= TOL
+    plan.close()
