@@ -237,3 +237,25 @@ def test_wide_router_layer(T):
     assert np.array_equal(r["counts"], counts) and np.array_equal(r["perm"], perm)
     assert _rel_err(_bf16_bits_to_f64(y), ref) <= TOL
     plan.close()
+
+
+# H with 17 column blocks of 256: gate/up tasks split into two units (9 + 8
+# blocks) whose partial sums carry across the units
+LONGH = W.Workload("decode-long-h", 1, 16, 4352, 256, 2, (3,), 3, 128, W.SC_BF16, "plain")
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_split_gate_up_task(T):
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = LONGH
+    plan, info = harness.build_plan(wl)
+    wr, bias, _ = info["routers"][0]
+    experts = [_oracle_expert(wl, 0, e) for e in range(wl.experts)]
+    x = W.tokens(wl, 400 + T, 0, T)
+    y, r = _run(plan, 0, x, wl)
+    ref = oracle.layer_forward(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                               wl.scale_dtype, x, wr, bias)
+    assert np.array_equal(r["logits"], ref["logits"])
+    assert np.array_equal(r["topk_idx"], ref["idx"])
+    assert _rel_err(_bf16_bits_to_f64(y), ref["y"]) <= TOL
+    plan.close()

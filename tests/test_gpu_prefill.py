@@ -192,3 +192,21 @@ def test_prefill_wide_router():
                                       wl.scale_dtype, x, wr, bias, np.arange(T))
     assert _rel_err(y, ref) <= TOL
     plan.close()
+
+
+def test_prefill_hidden_17_blocks():
+    """H = 4352 (17 code blocks of 256 columns, 68 stages per gate/up unit)."""
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = W.Workload("prefill-long-h", 1, 16, 4352, 256, 2, (24,), 3, 128, W.SC_BF16, "plain")
+    T = 24
+    plan, info = harness.build_plan(wl, max_tokens=T)
+    wr, bias, _ = info["routers"][0]
+    experts = [_oracle_expert(wl, 0, e) for e in range(wl.experts)]
+    x = W.tokens(wl, 5, 0, T)
+    y, r = _run(plan, x, wl)
+    ref = oracle.layer_forward(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                               wl.scale_dtype, x, wr, bias)
+    assert np.array_equal(r["logits"], ref["logits"])
+    assert np.array_equal(r["perm"], ref["perm"])
+    assert _rel_err(y, ref["y"]) <= TOL
+    plan.close()
