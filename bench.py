@@ -494,7 +494,8 @@ def run_stack(args):
             xs[0].view(torch.int16).copy_(x0[st])
             for l in range(L):
                 plan.forward(l, xs[l], ys[l], stream=torch.cuda.current_stream())
-                xs[l + 1].copy_((ys[l].float() + noise[st, l]).to(torch.bfloat16))
+                synth.residual_bf16_device(ys[l].data_ptr(), noise[st, l].data_ptr(), T * H, xs[l + 1].data_ptr(),
+                                           torch.cuda.current_stream().cuda_stream)
 
         with torch.cuda.stream(stream):
             body(0)  # per-T launch configuration before capture
@@ -593,7 +594,8 @@ def run_cached(args):
         for l in range(L):
             plan.update_router_bias(l, bias_stage[l], stream=torch.cuda.current_stream())
             plan.forward(l, xs[l], ys[l], stream=torch.cuda.current_stream())
-            xs[l + 1].copy_((ys[l].float() + noise_stage[l]).to(torch.bfloat16))
+            synth.residual_bf16_device(ys[l].data_ptr(), noise_stage[l].data_ptr(), T * H, xs[l + 1].data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream)
         plan.step_end(stream=torch.cuda.current_stream())
 
     def stage(st):

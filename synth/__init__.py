@@ -62,6 +62,9 @@ def lib_gpu():
             for f in (L.synth_gpu_normal_f32, L.synth_gpu_normal_bf16):
                 f.argtypes = [u64, u64, i64, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
                 f.restype = ctypes.c_int
+            L.synth_gpu_residual_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_void_p,
+                                                  ctypes.c_void_p]
+            L.synth_gpu_residual_bf16.restype = ctypes.c_int
             _lib_gpu = L
     return _lib_gpu
 
@@ -77,6 +80,14 @@ def normal_bf16_device(k: int, n: int, sigma: float, out_ptr: int, stream_ptr: i
     rc = lib_gpu().synth_gpu_normal_bf16(k, start, n, sigma, out_ptr, stream_ptr)
     if rc:
         raise RuntimeError(f"synth_gpu_normal_bf16 failed ({rc})")
+
+
+def residual_bf16_device(y_ptr: int, noise_ptr: int, n: int, out_ptr: int, stream_ptr: int = 0):
+    """out = bf16(float(y) + noise) on the device (bf16 y, fp32 noise, n elements): the
+    next layer's input of the chained-layer workloads, one kernel on `stream_ptr`."""
+    rc = lib_gpu().synth_gpu_residual_bf16(y_ptr, noise_ptr, n, out_ptr, stream_ptr)
+    if rc:
+        raise RuntimeError(f"synth_gpu_residual_bf16 failed ({rc})")
 
 
 def lib():

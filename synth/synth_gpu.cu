@@ -61,3 +61,26 @@ extern "C" int synth_gpu_normal_bf16(uint64_t key, uint64_t start, int64_t n, fl
   normal_bf16_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(key, start, n, multiplier(sigma), out);
   return (int)cudaGetLastError();
 }
+
+/* Stacked-layer input: out[i] = bf16(float(y[i]) + noise[i]) (fp32 add, round to
+   nearest even; NaN to the canonical quiet NaN), the next layer's input in the
+   chained-layer workloads. */
+__global__ void residual_bf16_kernel(const uint16_t* y, const float* noise, int64_t n, uint16_t* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t u = __float_as_uint(__fadd_rn(__uint_as_float((uint32_t)y[i] << 16), noise[i]));
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) {
+      out[i] = 0x7FC0;
+      continue;
+    }
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    out[i] = (uint16_t)(u >> 16);
+  }
+}
+
+extern "C" int synth_gpu_residual_bf16(const uint16_t* y, const float* noise, int64_t n, uint16_t* out,
+                                       void* stream) {
+  if (n <= 0) return 0;
+  const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  residual_bf16_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(y, noise, n, out);
+  return (int)cudaGetLastError();
+}

@@ -35,3 +35,20 @@ def test_expert_master_on_device():
                             torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(d.cpu().numpy().reshape(r, c), W.expert_master(wl, 5, 17, 2))
+
+
+def test_residual_bf16_matches_torch():
+    """The chained-layer input bf16(float(y) + noise), one device kernel, bit for bit
+    the value of the same fp32 add rounded by torch."""
+    import torch
+    import synth
+    n = 3 * 4096 + 7
+    g = torch.Generator(device="cpu").manual_seed(3)
+    y = (torch.randn(n, generator=g) * 4).to(torch.bfloat16).cuda()
+    noise = torch.randn(n, generator=g).cuda()
+    out = torch.empty_like(y)
+    synth.residual_bf16_device(y.data_ptr(), noise.data_ptr(), n, out.data_ptr(),
+                               torch.cuda.current_stream().cuda_stream)
+    ref = (y.float() + noise).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
