@@ -11,7 +11,8 @@
 //        lower expert index), the renormalised softmax weights, the grouping
 //        of (token, expert) pairs by expert and the residence of each distinct
 //        expert (an HBM slot, or pinned host memory read in place over UVA);
-//        CTA 0 alone writes the routing outputs and the cache accounting;
+//        CTA 0's producer warp alone writes the routing outputs and the
+//        cache accounting, once it has issued its units;
 //      - then runs its share of the work:
 //          A task (expert d, 16 rows of I): gate and up projections of those
 //            rows for the expert's tokens, streamed as NP units (column
@@ -242,27 +243,36 @@ __device__ __forceinline__ unsigned long long tagged(uint32_t payload, uint32_t 
   return (unsigned long long)payload | ((unsigned long long)epoch << 32);
 }
 
-// Payload of a hand-off word once it carries `epoch` (v = a first read of it).
-// Bounded: after ~2^22 polls (well over a second) it latches a timeout in the
-// plan's error word and returns 0, so the kernel always ends.
-__device__ __noinline__ uint32_t wait_tagged(const unsigned long long* p, unsigned long long v,
-                                             uint32_t epoch, uint32_t* err) {
-  for (uint32_t it = 0; (uint32_t)(v >> 32) != epoch; ++it) {
+// Waits (bounded) until each word q of p(q) = base + q*stride with bit q of
+// `valid` set carries `epoch`; v holds their first reads.  All stale words are
+// read again together, so a wait costs one round trip per poll.  After ~2^22
+// polls (well over a second) it latches a timeout in the plan's error word and
+// the stale payloads read as 0, so the kernel always ends.
+template <int N>
+__device__ __forceinline__ void wait_words(const unsigned long long* base, int64_t stride, unsigned valid,
+                                           uint32_t epoch, uint32_t* err, unsigned long long (&v)[N]) {
+  for (uint32_t it = 0;; ++it) {
+    unsigned stale = 0u;
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+      if (((valid >> q) & 1u) && (uint32_t)(v[q] >> 32) != epoch) stale |= 1u << q;
+    if (!stale) return;
     // give up at once if another wait of this forward already timed out
-    if ((it & 4095u) == 4095u && *reinterpret_cast<volatile uint32_t*>(err)) return 0u;
-    if (it >= (1u << 22)) {
-      *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout;
-      __threadfence_system();
-      return 0u;
+    if (it >= (1u << 22) || ((it & 4095u) == 4095u && *reinterpret_cast<volatile uint32_t*>(err))) {
+      if (it >= (1u << 22)) {
+        *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout;
+        __threadfence_system();
+      }
+#pragma unroll
+      for (int q = 0; q < N; ++q)
+        if ((stale >> q) & 1u) v[q] = 0ull;
+      return;
     }
-    __nanosleep(it < 64 ? 32 : 256);
-    v = ld_relaxed_u64(p);
+    if (it >= 64) __nanosleep(128);
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+      if ((stale >> q) & 1u) v[q] = ld_relaxed_u64(base + q * stride);
   }
-  return (uint32_t)v;
-}
-__device__ __forceinline__ uint32_t payload_of(const unsigned long long* p, unsigned long long v,
-                                               uint32_t epoch, uint32_t* err) {
-  return (uint32_t)(v >> 32) == epoch ? (uint32_t)v : wait_tagged(p, v, epoch, err);
 }
 
 // B-operand rows in shared memory are kept in fragment order: for column
@@ -415,6 +425,16 @@ expert_decode_kernel(ExpertArgs a) {
     }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  // Softmax over a token's k logits (R.w[t*k + j], j < k, descending), one
+  // lane per slot: w_j = exp(l_j - l_0) / sum_j exp(l_j - l_0), the sum in j order.
+  auto renormalise = [&](int t) {
+    __syncwarp();
+    const float l0 = R.w[t * k];
+    const float ex = lane < k ? expf(R.w[t * k + lane] - l0) : 0.f;
+    float z = 0.f;
+    for (int j = 0; j < k; ++j) z += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) R.w[t * k + lane] = ex / z;
+  };
   // ---- top-k, one warp per token.  E <= 512: every lane holds the logits of
   // experts lane, lane+32, ...; each of the k rounds takes the lane's best
   // untaken logit (lowest index among equals), then a warp max over an
@@ -455,17 +475,7 @@ expert_decode_kernel(ExpertArgs a) {
         R.w[t * k + j] = wv;  // logit for now
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      const float l0 = R.w[t * k];
-      float ex[kMaxTopK];
-      float z = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        ex[j] = expf(R.w[t * k + j] - l0);
-        z += ex[j];
-      }
-      for (int j = 0; j < k; ++j) R.w[t * k + j] = ex[j] / z;
-    }
+    renormalise(t);
   }
   // ---- larger E: each lane keeps its own best 8 (logit desc, index asc)
   // over experts lane, lane+32, ...; then k rounds of warp argmax
@@ -532,17 +542,7 @@ expert_decode_kernel(ExpertArgs a) {
         R.w[t * k + j] = bv;  // logit for now
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      const float l0 = R.w[t * k];
-      float ex[kMaxTopK];
-      float z = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        ex[j] = expf(R.w[t * k + j] - l0);
-        z += ex[j];
-      }
-      for (int j = 0; j < k; ++j) R.w[t * k + j] = ex[j] / z;
-    }
+    renormalise(t);
   }
   for (int i = tid; i < T * ngH; i += blockDim.x) {
     const int t = i / ngH, grp = i % ngH;
@@ -559,11 +559,16 @@ expert_decode_kernel(ExpertArgs a) {
     const int key0 = s0 < n ? R.e[s0] * T + s0 / k : 0x7fffffff;  // unique per slot
     const int key1 = s1 < n ? R.e[s1] * T + s1 / k : 0x7fffffff;
     int r0 = 0, r1 = 0;
+    if (n <= 32) {  // rank = number of smaller keys
+#pragma unroll 8
+      for (int j = 0; j < n; ++j) r0 += __shfl_sync(kAll, key0, j) < key0;
+    } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {  // rank = number of smaller keys
-      const int o0 = __shfl_sync(kAll, key0, j), o1 = __shfl_sync(kAll, key1, j);
-      r0 += (o0 < key0) + (o1 < key0);
-      r1 += (o0 < key1) + (o1 < key1);
+      for (int j = 0; j < 32; ++j) {
+        const int o0 = __shfl_sync(kAll, key0, j), o1 = __shfl_sync(kAll, key1, j);
+        r0 += (o0 < key0) + (o1 < key0);
+        r1 += (o0 < key1) + (o1 < key1);
+      }
     }
     if (s0 < n) {
       R.rank[s0] = r0;
@@ -617,9 +622,10 @@ expert_decode_kernel(ExpertArgs a) {
   __syncthreads();
   const int D = R.D;
 
-  // ---- CTA 0: routing outputs and accounting (off the critical path of the others)
-  if (blockIdx.x == 0) {
-    for (int s = tid; s < n; s += blockDim.x) {
+  // ---- routing outputs and cache accounting: CTA 0's producer warp, once
+  // it has issued its units (no other work depends on them in this forward)
+  auto account = [&]() {
+    for (int s = lane; s < n; s += 32) {
       a.topk_idx[s] = R.e[s];
       a.topk_w[s] = R.w[s];
       a.perm[s] = R.perm[s];
@@ -630,7 +636,7 @@ expert_decode_kernel(ExpertArgs a) {
       if (a.dbg.inv) a.dbg.inv[s] = R.rank[s];
     }
     if (a.dbg.counts || a.dbg.offsets) {
-      for (int ee = tid; ee <= E; ee += blockDim.x) {
+      for (int ee = lane; ee <= E; ee += 32) {
         int below = 0, eq = 0;
         for (int q = 0; q < n; ++q) {
           below += R.e[q] < ee;
@@ -641,9 +647,9 @@ expert_decode_kernel(ExpertArgs a) {
       }
     }
     if (a.dbg.logits)
-      for (int i = tid; i < T * E; i += blockDim.x) a.dbg.logits[i] = __ldcg(a.logits + i);
+      for (int i = lane; i < T * E; i += 32) a.dbg.logits[i] = __ldcg(a.logits + i);
     if (a.lfu) {
-      for (int d = tid; d < D; d += blockDim.x) {  // distinct experts: no two threads share g
+      for (int d = lane; d < D; d += 32) {  // distinct experts: no two threads share g
         const int64_t gid = a.ge0 + R.wl_e[d];
         a.lfu_count[gid] += 1u;
         a.lfu_last[gid] = *a.step;
@@ -653,7 +659,7 @@ expert_decode_kernel(ExpertArgs a) {
         }
       }
     }
-    if (tid == 0) {
+    if (lane == 0) {
       unsigned long long* st = a.stats;
       const int nh = R.nh;
       const unsigned long long v0 = st[kStatAccesses], v1 = st[kStatHits], v2 = st[kStatMisses],
@@ -667,7 +673,7 @@ expert_decode_kernel(ExpertArgs a) {
       st[kStatPairs] = v5 + n;
       st[kStatForwards] = v6 + 1;
     }
-  }
+  };
 
   // ---- work
   const uint32_t epoch = *reinterpret_cast<const volatile unsigned*>(a.epoch);
@@ -795,6 +801,7 @@ expert_decode_kernel(ExpertArgs a) {
       if (use > 0) mbar_wait(smem_addr(&emptyb[sl]), (uint32_t)(use - 1) & 1u, a.err);
       issue(i, sl, hostmask);
     }
+    if (blockIdx.x == 0) account();
     cp_async_wait<0>();
     return;
   }
@@ -814,17 +821,21 @@ expert_decode_kernel(ExpertArgs a) {
       const unsigned long long* hsrc = a.hbuf + (int64_t)d * a.tstride * np2;
       for (int i0 = tid; i0 < Te * np2; i0 += 4 * kWarps * 32) {
         unsigned long long v[4];
+        unsigned valid = 0u;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // four reads in flight
+        for (int q = 0; q < 4; ++q) {  // four reads in flight, waited on together
           const int ii = i0 + q * kWarps * 32;
-          v[q] = (ii < Te * np2 && ii % np2 < ip2) ? ld_relaxed_u64(hsrc + ii) : 0ull;
+          const bool ok = ii < Te * np2 && ii % np2 < ip2;
+          v[q] = ok ? ld_relaxed_u64(hsrc + ii) : 0ull;
+          valid |= (unsigned)ok << q;
         }
+        wait_words<4>(hsrc + i0, kWarps * 32, valid, epoch, a.err, v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int ii = i0 + q * kWarps * 32;
           if (ii < Te * np2) {
             const int n = ii / np2, c = ii % np2;
-            const uint32_t pr = c < ip2 ? payload_of(hsrc + ii, v[q], epoch, a.err) : 0u;
+            const uint32_t pr = c < ip2 ? (uint32_t)v[q] : 0u;
             *reinterpret_cast<uint32_t*>(hs + (size_t)n * hrow + frag_offset(2 * c)) = pr;
           }
         }
@@ -965,13 +976,13 @@ expert_decode_kernel(ExpertArgs a) {
         const int t = i2 / kBRows, row = rb * kBRows + i2 % kBRows;
         unsigned long long v[kMaxTopK];
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)  // all k reads in flight, then summed in j order
+        for (int j = 0; j < kMaxTopK; ++j)  // all k reads in flight, waited on together, summed in j order
           if (j < k) v[j] = ld_relaxed_u64(a.obuf + (int64_t)(t * k + j) * H + row);
+        wait_words<kMaxTopK>(a.obuf + (int64_t)(t * k) * H + row, H, (1u << k) - 1u, epoch, a.err, v);
         float o = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
-          if (j < k)
-            o += __uint_as_float(payload_of(a.obuf + (int64_t)(t * k + j) * H + row, v[j], epoch, a.err));
+          if (j < k) o += __uint_as_float((uint32_t)v[j]);
         a.y[(int64_t)t * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
       }
     }
