@@ -533,7 +533,7 @@ def run_stack(args):
                          "host_GB_per_step": ob / 1e9, "weight_stream_GBps": (hb + ob) / (ms * 1e-3) / 1e9,
                          "roofline_ms": roof * 1e3, "roofline_frac": roof / (ms * 1e-3),
                          "roofline_frac_max_form": roof_max / (ms * 1e-3), "clocks": ck}
-        launches = 2 * L * args.steps
+        launches = 3 * L * args.steps  # router, expert kernel, next layer's input
         del graphs
     T_head = str(max(wl.tokens))
     line = _common_line(
@@ -591,8 +591,8 @@ def run_cached(args):
 
     def body():
         xs[0].view(torch.int16).copy_(x_stage)
+        plan.update_router_biases(0, bias_stage, stream=torch.cuda.current_stream())
         for l in range(L):
-            plan.update_router_bias(l, bias_stage[l], stream=torch.cuda.current_stream())
             plan.forward(l, xs[l], ys[l], stream=torch.cuda.current_stream())
             synth.residual_bf16_device(ys[l].data_ptr(), noise_stage[l].data_ptr(), T * H, xs[l + 1].data_ptr(),
                                        torch.cuda.current_stream().cuda_stream)
@@ -655,7 +655,7 @@ def run_cached(args):
          "second_half_ms_per_step": m2.elapsed_time(b) / (S - half),
          "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
                   "gpu": _numa_node(0)},
-         "setup_s": build_s, "gpu_launches": (2 * L + 2) * S, "clocks": ck})
+         "setup_s": build_s, "gpu_launches": (3 * L + 2) * S, "clocks": ck})  # per layer: router, expert kernel, next input; step end: 2
     print(json.dumps(line), flush=True)
     plan.close()
 

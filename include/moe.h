@@ -149,6 +149,13 @@ moe_status moe_set_router(moe_plan* plan, int layer, const uint16_t* wr_bf16, co
  * per-step bias updates without a synchronisation. */
 moe_status moe_update_router_bias(moe_plan* plan, int layer, const float* bias, void* stream);
 
+/* The same for layers first .. first+count-1 at once: bias [count][E] fp32,
+ * row i for layer first+i, in one stream-ordered copy (the biases of all
+ * layers sit contiguously in device memory).  MOE_ERR_INVALID for a layer
+ * range outside [0, num_layers) or bias NULL; count == 0 does nothing. */
+moe_status moe_update_router_biases(moe_plan* plan, int first, int count, const float* bias,
+                                    void* stream);
+
 /* Place experts first .. first+count-1 of `layer`: copy each expert from the
  * canonical format into its device layout at residence[i] (MOE_RES_HBM or
  * MOE_RES_HOST; ignored under LFU, where every expert goes to host memory;

@@ -25,6 +25,7 @@ POLICY_STATIC, POLICY_LFU = 0, 1
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_set_router", "moe_update_router_bias",
+           "moe_update_router_biases",
            "moe_place_experts", "moe_layer_forward", "moe_layer_forward_host", "moe_step_end",
            "moe_cache_stats", "moe_residence_table", "moe_quantize", "moe_probe_bandwidth",
            "moe_route_noalloc", "moe_status_string", "moe_last_error"]
@@ -81,6 +82,7 @@ def lib():
         L.moe_plan_destroy.argtypes = [_P]
         L.moe_set_router.argtypes = [_P, i32, _P, _P]
         L.moe_update_router_bias.argtypes = [_P, i32, _P, _P]
+        L.moe_update_router_biases.argtypes = [_P, i32, i32, _P, _P]
         L.moe_place_experts.argtypes = [_P, i32, i32, i32, _P, ctypes.POINTER(ExpertWeights)]
         L.moe_layer_forward.argtypes = [_P, i32, _P, i32, _P, _P, ctypes.POINTER(RoutingOut)]
         L.moe_layer_forward_host.argtypes = [_P, i32, _P, i32, _P, _P]
@@ -170,6 +172,11 @@ class Plan:
 
     def update_router_bias(self, layer, bias, stream=None):
         _check(lib().moe_update_router_bias(self._h, layer, _addr(bias), _stream(stream)), self._h)
+
+    def update_router_biases(self, first, bias, stream=None):
+        """bias: [count][E] fp32 (host or device) for layers first .. first+count-1."""
+        _check(lib().moe_update_router_biases(self._h, first, int(bias.shape[0]), _addr(bias),
+                                              _stream(stream)), self._h)
 
     def place_experts(self, layer, first, weights, residence=None):
         """weights: list of (codes[3], scales[3]) per expert (numpy or torch)."""

@@ -92,7 +92,8 @@ struct Plan {
 
   // routers
   std::vector<uint16_t*> wr;  // device [E][H] bf16 per layer
-  std::vector<float*> bias;   // device [E] per layer (zeros when none)
+  std::vector<float*> bias;   // device [E] per layer (zeros when none), rows of bias_all
+  float* bias_all = nullptr;  // device [L][E]
 
   // forward scratch (device)
   float* logits = nullptr;            // [maxT][E]

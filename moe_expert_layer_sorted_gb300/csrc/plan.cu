@@ -338,7 +338,7 @@ void release(Plan* p) {
   if (!p) return;
   cudaDeviceSynchronize();
   for (auto* w : p->wr) cudaFree(w);
-  for (auto* b : p->bias) cudaFree(b);
+  cudaFree(p->bias_all);
   void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
                  p->wl_blob, p->ctl, p->hbuf, p->obuf, p->pf_h, p->pf_o, p->pf_bucket, p->xsum, p->x_stage,
@@ -492,14 +492,20 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
 #undef ALLOC
   p->wr.assign(d.num_layers, nullptr);
   p->bias.assign(d.num_layers, nullptr);
+  if (dalloc(&p->bias_all, (int64_t)d.num_layers * E) != cudaSuccess) {
+    cudaGetLastError();
+    release(p);
+    return fail(nullptr, MOE_ERR_OOM, "router allocation failed");
+  }
+  cudaMemset(p->bias_all, 0, (size_t)d.num_layers * E * 4);
   for (int l = 0; l < d.num_layers; ++l) {
-    if (dalloc(&p->wr[l], E * H) != cudaSuccess || dalloc(&p->bias[l], E) != cudaSuccess) {
+    p->bias[l] = p->bias_all + (int64_t)l * E;
+    if (dalloc(&p->wr[l], E * H) != cudaSuccess) {
       cudaGetLastError();
       release(p);
       return fail(nullptr, MOE_ERR_OOM, "router allocation failed");
     }
     cudaMemset(p->wr[l], 0, E * H * 2);
-    cudaMemset(p->bias[l], 0, E * 4);
   }
   cudaMemset(p->blob_hbm, 0, LE * sizeof(void*));
   cudaMemset(p->blob_host, 0, LE * sizeof(void*));
@@ -568,6 +574,21 @@ extern "C" moe_status moe_update_router_bias(moe_plan* plan, int layer, const fl
   if (layer < 0 || layer >= p->d.num_layers || !bias) return fail(p, MOE_ERR_INVALID, "bad layer or bias");
   DeviceScope ds(p->d.device);
   CK(p, cudaMemcpyAsync(p->bias[layer], bias, (size_t)p->d.num_experts * 4, cudaMemcpyDefault,
+                        (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_update_router_biases(moe_plan* plan, int first, int count, const float* bias,
+                                               void* stream) {
+  Plan* p = reinterpret_cast<Plan*>(plan);
+  if (!p) return fail(nullptr, MOE_ERR_INVALID, "plan is NULL");
+  Busy b(p);
+  if (!b.ok) return fail(p, MOE_ERR_STATE, "plan is in use by another thread");
+  if (first < 0 || count < 0 || first > p->d.num_layers - count || !bias)
+    return fail(p, MOE_ERR_INVALID, "bad layer range or bias");
+  if (count == 0) return MOE_OK;
+  DeviceScope ds(p->d.device);
+  CK(p, cudaMemcpyAsync(p->bias[first], bias, (size_t)count * p->d.num_experts * 4, cudaMemcpyDefault,
                         (cudaStream_t)stream));
   return MOE_OK;
 }

@@ -7,7 +7,8 @@ router bias) runs step by step through the C-ABI.  The distinct experts each
 forward routes to are read back and replayed through ``oracle.cache_sim``:
 per-(step, layer) hits and misses, admissions, evictions and the final slot
 owners must match exactly.  Layer outputs must be bit-identical to a plan
-that keeps every expert in HBM (placement changes no output bit)."""
+that keeps every expert in HBM (placement changes no output bit) and takes
+each step's drifted router biases in one call for all layers."""
 import numpy as np
 import pytest
 
@@ -55,10 +56,10 @@ def test_lfu_matches_cache_simulator():
             hits[s, l], misses[s, l] = st["hits"], st["misses"]
             assert st["accesses"] == len(d)
         plan.step_end()
-        for l in range(L):  # the same drift on both plans
+        for l in range(L):  # the same drift on both plans: one layer at a time, and all layers at once
             biases[l] = biases[l] + W.bias_drift(WL, s, l)
             plan.update_router_bias(l, biases[l])
-            ref.update_router_bias(l, biases[l])
+        ref.update_router_biases(0, np.ascontiguousarray(np.stack(biases), dtype=np.float32))
     torch.cuda.synchronize()
     sim = oracle.cache_sim(L, E, C, access)
     np.testing.assert_array_equal(hits, sim["hits"])
