@@ -66,6 +66,25 @@ constexpr int kRtStages = 4;             // 256-column blocks in flight (cp.asyn
 constexpr size_t kRtStageBytes = (size_t)(kRtTok + kRtExp) * 32 * 16;
 constexpr size_t kRtSmem = kRtStages * kRtStageBytes;
 
+// acc + x * w for the low (or high) bf16 halves of x and w, widened to fp32:
+// the product of two bf16 values is exact in fp32, so the one rounding of this
+// mixed-precision fma equals that of fmaf on the widened operands (bit for bit)
+// without the two widening instructions.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t x, uint32_t w, float c) {
+  asm("{\n .reg .b16 xl, xh, wl, wh;\n mov.b32 {xl, xh}, %1;\n mov.b32 {wl, wh}, %2;\n"
+      " fma.rn.f32.bf16 %0, xl, wl, %0;\n}"
+      : "+f"(c)
+      : "r"(x), "r"(w));
+  return c;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t x, uint32_t w, float c) {
+  asm("{\n .reg .b16 xl, xh, wl, wh;\n mov.b32 {xl, xh}, %1;\n mov.b32 {wl, wh}, %2;\n"
+      " fma.rn.f32.bf16 %0, xh, wh, %0;\n}"
+      : "+f"(c)
+      : "r"(x), "r"(w));
+  return c;
+}
+
 // Operands staged as bf16: row r of a 256-column block m holds, at uint4
 // index j, the elements 256m + 8j .. 256m + 8j + 7 (lane j's share in the
 // fixed order), so a lane's 16-byte reads are conflict-free.  A ring of
@@ -119,21 +138,15 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const uint16_t* __restri
       for (int b = 0; b < 8; ++b) wv[b] = reinterpret_cast<const uint2*>(&ws[(ew + b) * 32 + lane])[h];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        float xf[8], wf[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          const uint32_t u = (r < 2) ? xv[a].x : xv[a].y;
-          xf[a] = (r & 1) ? __uint_as_float(u & 0xffff0000u) : bf16f(u & 0xffffu);
-        }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          const uint32_t u = (r < 2) ? wv[b].x : wv[b].y;
-          wf[b] = (r & 1) ? __uint_as_float(u & 0xffff0000u) : bf16f(u & 0xffffu);
+          const uint32_t wu = (r < 2) ? wv[b].x : wv[b].y;
+#pragma unroll
+          for (int a = 0; a < 8; ++a) {
+            const uint32_t xu = (r < 2) ? xv[a].x : xv[a].y;
+            acc[a][b] = (r & 1) ? fma_bf16_hi(xu, wu, acc[a][b]) : fma_bf16_lo(xu, wu, acc[a][b]);
+          }
         }
-#pragma unroll
-        for (int a = 0; a < 8; ++a)
-#pragma unroll
-          for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xf[a], wf[b], acc[a][b]);
       }
     }
   }

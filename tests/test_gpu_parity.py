@@ -259,3 +259,42 @@ def test_split_gate_up_task(T):
     assert np.array_equal(r["topk_idx"], ref["idx"])
     assert _rel_err(_bf16_bits_to_f64(y), ref["y"]) <= TOL
     plan.close()
+
+
+# Router rows duplicated in pairs, or all equal: equal logits must go to the
+# lower expert index (the tie rule of the top-k), on both top-k paths of the
+# decode kernel (E <= 512 and E > 512)
+TIES = {384: W.Workload("decode-ties", 1, 384, 256, 128, 6, (8,), 3, 64, W.SC_BF16, "zipf", 1.0),
+        600: WIDE}
+
+
+@pytest.mark.parametrize("E", [384, 600])
+@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("mode", ["pairs", "all"])
+def test_router_ties_go_to_the_lower_index(E, T, mode):
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = TIES[E]
+    plan, info = harness.build_plan(wl)
+    wr, bias, _ = info["routers"][0]
+    wr, bias = wr.copy(), bias.copy()
+    if mode == "all":
+        wr[:] = wr[0]
+        bias[:] = bias[0]
+    else:
+        src = np.random.default_rng(7 + E + T).permutation(E)
+        for a_, b_ in zip(src[: E // 2], src[E // 2:]):  # expert b_ gets expert a_'s router row
+            wr[b_] = wr[a_]
+            bias[b_] = bias[a_]
+    plan.set_router(0, wr, bias)
+    x = W.tokens(wl, 500 + T, 0, T)
+    y, r = _run(plan, 0, x, wl)
+    lg = oracle.router_logits(x, wr, bias)
+    idx, w = oracle.topk(lg, wl.top_k)
+    assert np.array_equal(r["logits"], lg)
+    assert np.array_equal(r["topk_idx"], idx)
+    if mode == "all":
+        assert (idx == np.arange(wl.top_k)).all()
+    np.testing.assert_allclose(r["topk_w"], w, rtol=2e-6, atol=1e-7)
+    counts, offsets, perm, inv = oracle.permute(idx, wl.experts)
+    assert np.array_equal(r["perm"], perm) and np.array_equal(r["inv"], inv)
+    plan.close()
