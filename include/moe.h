@@ -238,6 +238,15 @@ moe_status moe_route_noalloc(const void* x_bf16, int T, int H, const void* wr_bf
                              const float* bias, int E, int k, int32_t* topk_idx, float* topk_w,
                              void* stream);
 
+/* Test hook for the failure path.  The next decode forward (T <= 8) of `plan`
+ * publishes none of its gate/up results, so every down-projection unit's
+ * bounded wait for them runs out (about a second): the kernel latches a
+ * timeout in the plan's error word and ends with wrong outputs; nothing
+ * faults or hangs.  The call after that forward returns MOE_ERR_TIMEOUT (and
+ * does nothing else); the plan is then usable again.  MOE_ERR_INVALID for
+ * plan NULL. */
+moe_status moe_debug_fail_next_forward(moe_plan* plan);
+
 const char* moe_status_string(moe_status s);
 /* Last error text of `plan` (or of the last call that had no plan, for NULL). */
 const char* moe_last_error(const moe_plan* plan);

@@ -25,7 +25,7 @@ POLICY_STATIC, POLICY_LFU = 0, 1
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_set_router", "moe_update_router_bias",
-           "moe_update_router_biases",
+           "moe_update_router_biases", "moe_debug_fail_next_forward",
            "moe_place_experts", "moe_layer_forward", "moe_layer_forward_host", "moe_step_end",
            "moe_cache_stats", "moe_residence_table", "moe_quantize", "moe_probe_bandwidth",
            "moe_route_noalloc", "moe_status_string", "moe_last_error"]
@@ -83,6 +83,7 @@ def lib():
         L.moe_set_router.argtypes = [_P, i32, _P, _P]
         L.moe_update_router_bias.argtypes = [_P, i32, _P, _P]
         L.moe_update_router_biases.argtypes = [_P, i32, i32, _P, _P]
+        L.moe_debug_fail_next_forward.argtypes = [_P]
         L.moe_place_experts.argtypes = [_P, i32, i32, i32, _P, ctypes.POINTER(ExpertWeights)]
         L.moe_layer_forward.argtypes = [_P, i32, _P, i32, _P, _P, ctypes.POINTER(RoutingOut)]
         L.moe_layer_forward_host.argtypes = [_P, i32, _P, i32, _P, _P]
@@ -172,6 +173,10 @@ class Plan:
 
     def update_router_bias(self, layer, bias, stream=None):
         _check(lib().moe_update_router_bias(self._h, layer, _addr(bias), _stream(stream)), self._h)
+
+    def debug_fail_next_forward(self):
+        """Test hook: the next decode forward's bounded waits run out (see include/moe.h)."""
+        _check(lib().moe_debug_fail_next_forward(self._h), self._h)
 
     def update_router_biases(self, first, bias, stream=None):
         """bias: [count][E] fp32 (host or device) for layers first .. first+count-1."""

@@ -229,6 +229,7 @@ struct ExpertArgs {
   float zcorr;  // 128 + 2^(b-1)
   uint32_t* err;
   int slot_bytes, nslots;
+  int skip_h;  // test hook: publish no h (the down units' waits run out)
 };
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
@@ -938,7 +939,7 @@ expert_decode_kernel(ExpertArgs a) {
           const float h = gv / (1.0f + expf(-gv)) * uv;
           const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(h));
           const uint32_t next = __shfl_down_sync(0xffffffffu, hb, 8);  // row + 1, same token slot
-          if (!(row & 1) && col < Te)  // bf16 pair (rows row, row + 1) of token slot col
+          if (!(row & 1) && col < Te && !a.skip_h)  // bf16 pair (rows row, row + 1) of token slot col
             st_relaxed_u64(a.hbuf + ((int64_t)d * a.tstride + col) * (KP / 2) + mt * 8 + (row >> 1),
                            tagged(hb | (next << 16), epoch));
         }
@@ -1118,6 +1119,8 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.sdt = d.scale_dtype;
   a.zcorr = zcorr;
   a.err = p.err_dev;
+  a.skip_h = p.fail_next ? 1 : 0;
+  p.fail_next = false;
   a.slot_bytes = cf.slot_bytes;
   a.nslots = cf.nslots;
   const int b = d.weight_bits, grid = cf.grid;

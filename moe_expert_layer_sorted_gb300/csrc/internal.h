@@ -149,6 +149,8 @@ struct Plan {
   } dcfg[kDecodeMaxTokens + 1];
   size_t dsmem_set = 0, rsmem_set = 0;  // largest max-dynamic-smem attributes set so far
 
+  bool fail_next = false;  // test hook: the next decode forward publishes no gate/up results
+
   std::atomic<int> busy{0};
   std::string last_error;
 };

@@ -578,6 +578,13 @@ extern "C" moe_status moe_update_router_bias(moe_plan* plan, int layer, const fl
   return MOE_OK;
 }
 
+extern "C" moe_status moe_debug_fail_next_forward(moe_plan* plan) {
+  Plan* p = reinterpret_cast<Plan*>(plan);
+  if (!p) return fail(nullptr, MOE_ERR_INVALID, "plan is NULL");
+  p->fail_next = true;
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_update_router_biases(moe_plan* plan, int first, int count, const float* bias,
                                                void* stream) {
   Plan* p = reinterpret_cast<Plan*>(plan);
@@ -722,9 +729,15 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
     if (!p->placed[base + e]) return fail(p, MOE_ERR_STATE, "every expert of the layer must be placed first");
   DeviceScope ds(p->d.device);
   if (*p->err_host) {
-    p->err_host[0] = 0;
     cudaDeviceSynchronize();
-    cudaMemset(p->ctl, 0, sizeof(Ctl));
+    p->err_host[0] = 0;
+    // epoch 0 and every hand-off word at epoch 0 again: no word written by an
+    // earlier forward can be taken as current by a later one
+    const int64_t decT = std::min<int64_t>(d.max_tokens, kDecodeMaxTokens);
+    cudaMemset(&p->ctl->epoch, 0, sizeof(unsigned));
+    cudaMemset(p->hbuf, 0, (size_t)p->max_distinct * decT * (p->lay.m[2].kpad / 2) * 8);
+    cudaMemset(p->obuf, 0, (size_t)decT * d.top_k * d.hidden * 8);
+    cudaDeviceSynchronize();
     return fail(p, MOE_ERR_TIMEOUT, "a bounded device-side wait of an earlier forward gave up");
   }
   cudaStream_t s = (cudaStream_t)stream;

@@ -61,6 +61,7 @@ def test_bad_descriptors_rejected_on_the_host():
     assert L.moe_plan_create(ctypes.byref(d), ctypes.byref(h)) == 1
     assert L.moe_plan_destroy(None) == 1
     assert L.moe_update_router_biases(None, 0, 1, None, None) == 1
+    assert L.moe_debug_fail_next_forward(None) == 1
     assert L.moe_quantize(None, 4, 4, 4, 4, 0, None, None, None) == 1
 
 

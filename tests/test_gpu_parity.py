@@ -298,3 +298,35 @@ def test_router_ties_go_to_the_lower_index(E, T, mode):
     counts, offsets, perm, inv = oracle.permute(idx, wl.experts)
     assert np.array_equal(r["perm"], perm) and np.array_equal(r["inv"], inv)
     plan.close()
+
+
+def test_bounded_wait_runs_out_and_the_plan_recovers():
+    """The failure path without a fault: a forward whose gate/up results are
+    never published runs its down units' bounded waits out and ends; the next
+    call reports MOE_ERR_TIMEOUT; after it the plan gives the oracle's routing
+    and outputs again, bit-identical to a forward before the failure."""
+    import moe_expert_layer_sorted_gb300 as M
+    from moe_expert_layer_sorted_gb300 import harness
+    torch = _torch()
+    wl = W.WORKLOADS["tiny"]
+    plan, info = harness.build_plan(wl)
+    wr, bias, _ = info["routers"][0]
+    T = 4
+    x = W.tokens(wl, 900, 0, T)
+    y0, _ = _run(plan, 0, x, wl)
+    plan.debug_fail_next_forward()
+    _run(plan, 0, x, wl)  # its waits run out (bounded), the kernel ends
+    with pytest.raises(M.MoeError) as ei:
+        _run(plan, 0, x, wl)
+    assert ei.value.status == 4  # MOE_ERR_TIMEOUT
+    y1, r = _run(plan, 0, x, wl)
+    assert torch.equal(y1.view(torch.int16), y0.view(torch.int16))
+    experts = [_oracle_expert(wl, 0, e) for e in range(wl.experts)]
+    ref = oracle.layer_forward(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                               wl.scale_dtype, x, wr, bias)
+    assert np.array_equal(r["topk_idx"], ref["idx"])
+    assert _rel_err(_bf16_bits_to_f64(y1), ref["y"]) <= TOL
+    for _ in range(3):  # and keeps working
+        y2, _ = _run(plan, 0, x, wl)
+        assert torch.equal(y2.view(torch.int16), y0.view(torch.int16))
+    plan.close()
