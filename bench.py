@@ -739,6 +739,97 @@ def run_prefill(args):
     plan.close()
 
 
+def run_cpu_vs_uva(args):
+    """The measured comparison of serving a host-resident expert: the GPU reading
+    it in place over its host link (the decode forward's extra time against the
+    same layer with every expert in HBM) against the host CPU computing the
+    expert's FFN (cpu_expert.c, on 1 thread and on every core).  Inputs: T = 1
+    decode-layer tokens that route to exactly one host-resident expert."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import cpu_expert, harness, probe_bandwidth
+    from synth import workloads as W
+    wl = W.WORKLOADS["decode"]
+    link_gbs, _ = probe_bandwidth(0, 1 << 30, 5)
+    plan, info = harness.build_plan(wl)
+    ref, _ = harness.build_plan(wl, all_hbm=True)
+    host = info["host_sets"][0]
+    k = wl.top_k
+    idx = torch.empty(1, k, dtype=torch.int32, device="cuda")
+    picks = []
+    for st in range(7000, 9000):
+        xb = W.tokens(wl, st, 0, 1)
+        x = torch.from_numpy(xb.view(np.int16).copy()).cuda().view(torch.bfloat16)
+        y = torch.empty_like(x)
+        plan.forward(0, x, y, dbg=dict(topk_idx=idx))
+        torch.cuda.synchronize()
+        hs = [int(e) for e in idx.cpu().numpy().ravel() if int(e) in host]
+        if len(hs) == 1:
+            picks.append((xb, x, hs[0]))
+        if len(picks) == args.cpu_vs_uva_picks:
+            break
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def fwd_us(p, x):
+        y = torch.empty_like(x)
+        with torch.cuda.stream(stream):
+            p.forward(0, x, y, stream=stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                p.forward(0, x, y, stream=torch.cuda.current_stream())
+        stream.synchronize()
+        ev = []
+        with torch.cuda.stream(stream):  # queued back to back: no idle gaps between the forwards
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                ev.append((a, b))
+        stream.synchronize()
+        return float(np.median([a.elapsed_time(b) * 1e3 for a, b in ev[args.warmup:]]))
+
+    cores = os.cpu_count() or 1
+    rows = []
+    for xb, x, e in picks:
+        t_host, t_hbm = fwd_us(plan, x), fwd_us(ref, x)
+        codes, scales = info["quantiser"].expert(0, e)
+        hc = [c.cpu().numpy() for c in codes]
+        hsc = [s.view(torch.int16).cpu().numpy() if s.dtype != torch.float32 else s.cpu().numpy() for s in scales]
+        cpu = {}
+        for n in (1, cores):
+            ts = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                cpu_expert.expert_ffn(hc, hsc, wl.hidden, wl.inter, wl.bits, wl.group, wl.scale_dtype, xb, threads=n)
+                ts.append((time.perf_counter() - t0) * 1e6)
+            cpu[n] = float(np.median(ts))
+        rows.append({"expert": e, "gpu_forward_us_with_host_expert": t_host, "gpu_forward_us_all_hbm": t_hbm,
+                     "gpu_extra_us": t_host - t_hbm, "cpu_expert_us_1_thread": cpu[1],
+                     f"cpu_expert_us_{cores}_threads": cpu[cores]})
+    med = lambda key: float(np.median([r[key] for r in rows]))
+    extra_us = med("gpu_extra_us")
+    line = _common_line(
+        args, "host-resident expert: GPU in-place read vs CPU compute (extra us per forward)", extra_us, "us",
+        med("gpu_forward_us_with_host_expert") / 1e3,
+        {"workload": wl.desc + "; T = 1 tokens routed to exactly one host-resident expert",
+         "l2": "256 MiB flush before each timed forward", "cuda_graph": True, "parallelism": "single GPU"},
+        {"higher_is_better": False,
+         "expert_bytes": 4915200, "link_GBps": link_gbs, "link_time_us": 4915200 / (link_gbs * 1e3),
+         "gpu_forward_us_with_host_expert": med("gpu_forward_us_with_host_expert"),
+         "gpu_forward_us_all_hbm": med("gpu_forward_us_all_hbm"),
+         "cpu_expert_us": {"1": med("cpu_expert_us_1_thread"), str(cores): med(f"cpu_expert_us_{cores}_threads")},
+         "cpu_cores": cores, "picks": rows,
+         "note": "the CPU figure would replace the link read only if it overlapped the GPU's HBM work "
+                 "completely: compare it with gpu_forward_us_all_hbm, not with gpu_extra_us",
+         "gpu_launches": 2 * 2 * len(rows) * args.steps})
+    print(json.dumps(line), flush=True)
+    plan.close()
+    ref.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -748,7 +839,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=3)
-    ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
+                                                              "cpu-vs-uva"])
+    ap.add_argument("--cpu-vs-uva-picks", type=int, default=6)
     ap.add_argument("--cached-steps", type=int, default=2048)
     ap.add_argument("--tokens", type=int, default=0, help="prefill: batch size (default 8192)")
     args = ap.parse_args()
@@ -762,6 +855,8 @@ def main():
         run_cached(args)
     elif args.workload == "prefill":
         run_prefill(args)
+    elif args.workload == "cpu-vs-uva":
+        run_cpu_vs_uva(args)
     else:
         run_ours(args)
 
