@@ -3,11 +3,12 @@
  * o = Wd h (fp32 arithmetic, h kept in fp32).
  *
  * This is the measured comparison of "CPU compute of a host-resident expert"
- * against the GPU reading that expert in place over its host link (the
- * CPU-side expert computation of "Running a 24k-expert MoE on a single 32 GB
- * card", section 2, and the `--n-cpu-moe` runs of "MoE offload with
- * llama.cpp").  It is not a path of the library, which has no CPU fallback;
- * only the benchmark and its test call it.
+ * against the GPU reading that expert in place over its host link (the CPU
+ * fill-in for cache misses of "Running a 24k-expert MoE on a single 32 GB
+ * card", section 2 "Tiering, not activation, makes it run", and the
+ * CPU-computed expert layers of "125B sparse model on one 32 GB consumer
+ * card", section "Conclusion first").  It is not a path of the library,
+ * which has no CPU fallback; only the benchmark and its test call it.
  *
  * Codes: weight i of a [rows][cols] matrix (row-major) occupies bits
  * [i*b, i*b + b) of a little-endian bit stream and holds u = q + 2^(b-1).
