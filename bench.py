@@ -243,6 +243,11 @@ def cpu_baseline(wl, tokens: int = 3, seed_base: int = 77):
     return tokens / dt, dt, f"{tokens} single-token forwards of the decode layer (routing + quantise + fp64 FFN of the routed experts)"
 
 
+DECODE_WORKLOAD = ("decode MoE layer: H=4096, I=1024, E=384, top-6, int3 G128 bf16 scales, Zipf(1.0), "
+                   "115 least-popular experts in pinned host memory (UVA), 269 in HBM; "
+                   "step = forwards at T=1, 4, 6")
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -266,10 +271,10 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode layer H=4096 I=1024 E=384 top-6 int3 G128 bf16 scales, "
-                                   "batch 1 (bounded CPU sample)"},
+            "config": {"workload": DECODE_WORKLOAD, "parallelism": "host CPU, 1 thread"},
             "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": 1,
-                             "sample": f"{args.steps} single-token forwards"},
+                             "sample": f"bounded sample of the workload: {args.steps} single-token forwards "
+                                       "(routing + quantise + fp64 FFN of the routed experts), one per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -415,9 +420,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; weights N(0,0.02) quantised by the library's GPU quantiser)",
-            "config": {"workload": "decode MoE layer: H=4096, I=1024, E=384, top-6, int3 G128 bf16 "
-                                   "scales, Zipf(1.0), 115 least-popular experts in pinned host "
-                                   "memory (UVA), 269 in HBM; step = forwards at T=1, 4, 6",
+            "config": {"workload": DECODE_WORKLOAD,
                        "tokens_per_step": tokens_step, "l2": "256 MiB flush between steps, outside the timed events",
                        "cuda_graph": use_graph, "parallelism": "replicas" if ws > 1 else "single GPU"},
             "weight_stream_GBps": achieved,
