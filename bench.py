@@ -220,6 +220,23 @@ def _dist():
     return ws, rank, local
 
 
+def replica_step_ms(ms_step: float, ws: int, device=None) -> float:
+    """Per-step time of the job when every rank runs one replica of the layer:
+    the maximum over the ranks (the job's step ends with its slowest rank)."""
+    if ws <= 1:
+        return ms_step
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(tokens_per_rank_step: int, ws: int, ms_step: float) -> float:
+    """Whole-job throughput: the tokens every rank processed per step over the job's step time."""
+    return ws * tokens_per_rank_step / (ms_step * 1e-3)
+
+
 def cpu_baseline(wl, tokens: int = 3, seed_base: int = 77):
     """The oracle (single-threaded C, fp64 FFN) on `tokens` single-token
     forwards of the workload: routing over the layer, then the routed experts
@@ -354,12 +371,9 @@ def run_ours(args):
     fw = max(st["forwards"], 1)
     hbm_b = st["hbm_bytes"] / args.steps     # per step (3 forwards)
     host_b = st["host_bytes"] / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = replica_step_ms(ms_step, ws, dev)
     tokens_step = sum(BATCHES)
-    value = ws * tokens_step / (ms_step * 1e-3)
+    value = replica_value(tokens_step, ws, ms_step)
     achieved = (hbm_b + host_b) / (ms_step * 1e-3) / 1e9
     roof_s = hbm_b / (hbm_peak * 1e9) + host_b / (link_gbs * 1e9)
     roof_max_s = max(hbm_b / (hbm_peak * 1e9), host_b / (link_gbs * 1e9))  # perfect link/HBM overlap
