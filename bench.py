@@ -847,6 +847,74 @@ def run_cpu_vs_uva(args):
     ref.close()
 
 
+def run_prefetch_bound(args):
+    """Upper bound of layer-ahead prefetch on the cached 48-layer decode: while
+    layer l runs, layer l+1's experts are predicted by layer l+1's router on
+    layer l's input (the only hidden state available that early); a prefetch of
+    the predicted experts could turn into hits at most the misses of layer l+1
+    that the prediction contains.  Counted over the second half of the steps
+    (the LFU cache warm), with the bench's own chained inputs and bias drift."""
+    import torch
+    import synth
+    from moe_expert_layer_sorted_gb300 import harness, route_noalloc
+    from synth import workloads as W
+    wl = W.WORKLOADS["cached"]
+    dev = torch.device("cuda", 0)
+    plan, info = harness.build_plan(wl, gpu_gen=True)
+    L, H, E, k, T = wl.layers, wl.hidden, wl.experts, wl.top_k, 1
+    S = args.prefetch_steps
+    b0 = np.stack([info["routers"][l][1] for l in range(L)]).astype(np.float32)
+    drift = np.stack([np.stack([W.bias_drift(wl, st, l) for l in range(L)]) for st in range(S)])
+    bias_steps = torch.from_numpy(np.concatenate([b0[None], b0[None] + np.cumsum(drift, axis=0, dtype=np.float32)[:-1]])).to(dev)
+    wr = [torch.from_numpy(info["routers"][l][0].view(np.int16).copy()).to(dev).view(torch.bfloat16) for l in range(L)]
+    cs = torch.cuda.current_stream().cuda_stream
+    xs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(L + 1)]
+    ys = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    noise = torch.empty(T, H, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    pidx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    pw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    acc = hits = misses = covered = pred_right = 0
+    t0 = time.perf_counter()
+    for st in range(S):
+        plan.update_router_biases(0, bias_steps[st])
+        synth.normal_bf16_device(W.key(wl.seed, W.TAG_X, st, 0), T * H, 1.0, xs[0].data_ptr(), cs)
+        pred = None
+        for l in range(L):
+            res = plan.residence(l)  # slot per expert at this step (-1: host only)
+            plan.forward(l, xs[l], ys[l], dbg=dict(topk_idx=idx))
+            if l + 1 < L:  # layer l+1's experts predicted from layer l's input
+                route_noalloc(xs[l], wr[l + 1], bias_steps[st][l + 1], k, pidx, pw)
+            synth.normal_f32_device(W.key(wl.seed, W.TAG_NOISE, st, l), T * H, 1.0, noise.data_ptr(), cs)
+            synth.residual_bf16_device(ys[l].data_ptr(), noise.data_ptr(), T * H, xs[l + 1].data_ptr(), cs)
+            torch.cuda.synchronize()
+            used = set(int(e) for e in idx.cpu().numpy().ravel())
+            if st >= S // 2:
+                miss = {e for e in used if res[e] < 0}
+                acc += len(used)
+                misses += len(miss)
+                hits += len(used) - len(miss)
+                if pred is not None:
+                    covered += len(miss & pred)
+                    pred_right += len(used & pred)
+            pred = set(int(e) for e in pidx.cpu().numpy().ravel()) if l + 1 < L else None
+        plan.step_end()
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    n_pred = (S - S // 2) * (L - 1) * k
+    line = _common_line(
+        args, "layer-ahead prefetch bound (cached 48-layer decode): hit rate with the predicted experts prefetched",
+        (hits + covered) / max(acc, 1), "fraction", elapsed * 1e3 / S,
+        {"workload": wl.desc.replace("2048 steps", f"{S} steps") + "; counted over the second half",
+         "predictor": "layer l+1's router on layer l's input (bf16), top-k", "parallelism": "single GPU"},
+        {"hit_rate_lfu": hits / max(acc, 1), "hit_rate_with_prefetch_bound": (hits + covered) / max(acc, 1),
+         "accesses": acc, "misses": misses, "misses_covered_by_prediction": covered,
+         "prediction_precision": pred_right / max(n_pred, 1), "note": "an upper bound: every predicted "
+         "miss assumed fetched in time; the prefetch itself is not built", "gpu_launches": None})
+    print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -857,7 +925,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
-                                                              "cpu-vs-uva"])
+                                                              "cpu-vs-uva", "prefetch-bound"])
+    ap.add_argument("--prefetch-steps", type=int, default=512)
     ap.add_argument("--cpu-vs-uva-picks", type=int, default=6)
     ap.add_argument("--cached-steps", type=int, default=2048)
     ap.add_argument("--tokens", type=int, default=0, help="prefill: batch size (default 8192)")
@@ -874,6 +943,8 @@ def main():
         run_prefill(args)
     elif args.workload == "cpu-vs-uva":
         run_cpu_vs_uva(args)
+    elif args.workload == "prefetch-bound":
+        run_prefetch_bound(args)
     else:
         run_ours(args)
 
