@@ -915,6 +915,74 @@ def run_prefetch_bound(args):
     plan.close()
 
 
+def run_prefill_staging(args):
+    """Prefill with host-resident experts: the tcgen05 GEMMs reading the host
+    experts' codes in place over the link (bulk-copy warp, 16-byte cp.async)
+    against the same layer with every expert in HBM plus one host-to-HBM copy
+    of those experts' bytes (what staging them into reserved HBM slots before
+    the GEMMs would cost).  Shape of the cached decode's layer (H=2048, I=512,
+    E=512, top-8, int2 G64 fp16, Zipf(1.2)), T = 8192, the 154 (30 %)
+    least-popular experts in pinned host memory."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    from synth import workloads as W
+    wl = W.Workload("prefill-staging", 1, 512, 2048, 512, 8, (8192,), 2, 64, W.SC_F16, "zipf", 1.2,
+                    host_total=154, desc="prefill layer of the cached decode's shape: T=8192, H=2048, I=512, "
+                                         "E=512, top-8, int2 G64 fp16 scales, Zipf(1.2), 154 least-popular "
+                                         "experts in pinned host memory")
+    T = 8192
+    eb = sum(wl.codes_bytes(m) + wl.matrix_shape(m)[0] * (wl.matrix_shape(m)[1] // wl.group) * 2 for m in range(3))
+    x = torch.from_numpy(W.tokens(wl, 0, 0, T).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+
+    def time_fwd(plan):
+        for _ in range(args.warmup):
+            plan.forward(0, x, y)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            plan.forward(0, x, y)
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    plan, info = harness.build_plan(wl, max_tokens=T, gpu_gen=True)
+    n_host = len(info["host_sets"][0])
+    t_inplace = time_fwd(plan)
+    plan.close()
+    plan, _ = harness.build_plan(wl, max_tokens=T, gpu_gen=True, all_hbm=True)
+    t_hbm = time_fwd(plan)
+    plan.close()
+    nbytes = n_host * eb
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    cts = []
+    for i in range(args.warmup + args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            cts.append(a.elapsed_time(b))
+    t_copy = float(np.median(cts))
+    line = _common_line(
+        args, "prefill with host-resident experts: in-place reads vs staging into HBM (ms per forward)",
+        t_inplace, "ms", t_inplace,
+        {"workload": wl.desc, "tokens_per_step": T, "parallelism": "single GPU"},
+        {"higher_is_better": False, "ms_in_place": t_inplace, "ms_all_hbm": t_hbm, "ms_copy_host_experts": t_copy,
+         "ms_staged_serial": t_hbm + t_copy, "host_experts": n_host, "host_bytes": nbytes,
+         "copy_GBps": nbytes / (t_copy * 1e-3) / 1e9, "gpu_launches": None,
+         "note": "staging pays off if ms_all_hbm + ms_copy_host_experts (or the copy overlapped with the "
+                 "HBM experts' work) is below ms_in_place"})
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -925,7 +993,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
-                                                              "cpu-vs-uva", "prefetch-bound"])
+                                                              "cpu-vs-uva", "prefetch-bound",
+                                                              "prefill-staging"])
     ap.add_argument("--prefetch-steps", type=int, default=512)
     ap.add_argument("--cpu-vs-uva-picks", type=int, default=6)
     ap.add_argument("--cached-steps", type=int, default=2048)
@@ -945,6 +1014,8 @@ def main():
         run_cpu_vs_uva(args)
     elif args.workload == "prefetch-bound":
         run_prefetch_bound(args)
+    elif args.workload == "prefill-staging":
+        run_prefill_staging(args)
     else:
         run_ours(args)
 
