@@ -18,6 +18,7 @@ import numpy as np
 
 from . import (TAG_BIAS, TAG_DRIFT, TAG_NOISE, TAG_ROUTER, TAG_WEIGHT, TAG_X, key, normal_bf16,
                normal_f32, zipf_bias)
+from .popularity import calibrated_rank_bias
 
 SC_F32, SC_BF16, SC_F16 = 0, 1, 2
 GATE, UP, DOWN = 0, 1, 2
@@ -111,22 +112,32 @@ def expert_master(wl: Workload, layer: int, expert: int, m: int) -> np.ndarray:
     return normal_f32(key(wl.seed, TAG_WEIGHT, layer, expert, m), r * c, wl.w_sigma).reshape(r, c)
 
 
+def router_noise_sd() -> float:
+    """Standard deviation of the noise term x . Wr[e] of the "zipf" router for
+    x ~ N(0, 1): that of a standard Gumbel variable, pi / sqrt(6)."""
+    return math.pi / math.sqrt(6.0)
+
+
 def router(wl: Workload, layer: int):
     """(wr bf16 bits [E][H], bias fp32 [E] or None, popularity rank [E] or None).
 
     "plain": Wr ~ N(0, 0.05) rounded to bf16, no bias.
-    "zipf":  Wr ~ N(0, (pi / sqrt 6) / sqrt H), so that x.Wr for x ~ N(0,1) has the
-             spread of a standard Gumbel variable, plus bias[e] = log p_rank(e) with
-             p_r proportional to (r+1)^-s: the logits then act like Gumbel-perturbed
-             log-popularities, and top-k approximates drawing k experts without
-             replacement in proportion to a Zipf(s) popularity."""
+    "zipf":  Wr ~ N(0, sd / sqrt H) with sd = pi / sqrt 6, so that x . Wr[e] for
+             x ~ N(0,1) is close to independent N(0, sd^2) noise per expert;
+             expert e gets a seeded popularity rank and the bias of that rank
+             from synth.popularity.calibrated_rank_bias, for which top-k of
+             (bias + noise) includes every rank with its Plackett-Luce Zipf(s)
+             probability (k draws without replacement, p_r proportional to
+             (r+1)^-s)."""
     E, H = wl.experts, wl.hidden
     if wl.router == "plain":
         wr = normal_bf16(key(wl.seed, TAG_ROUTER, layer), E * H, 0.05).reshape(E, H)
         return wr, None, None
-    sigma = (math.pi / math.sqrt(6.0)) / math.sqrt(H)
-    wr = normal_bf16(key(wl.seed, TAG_ROUTER, layer), E * H, sigma).reshape(E, H)
-    bias, rank = zipf_bias(key(wl.seed, TAG_BIAS, layer), E, wl.zipf_s)
+    sd = router_noise_sd()
+    wr = normal_bf16(key(wl.seed, TAG_ROUTER, layer), E * H, sd / math.sqrt(H)).reshape(E, H)
+    _, rank = zipf_bias(key(wl.seed, TAG_BIAS, layer), E, wl.zipf_s)
+    by_rank, _ = calibrated_rank_bias(E, wl.top_k, float(wl.zipf_s), sd)
+    bias = np.asarray(by_rank, dtype=np.float32)[rank]
     return wr, bias, rank
 
 
