@@ -159,3 +159,43 @@ def test_cache_closed_forms_and_invariants():
     # frequency admission is not a stack algorithm in general, so only the
     # extremes are asserted)
     assert r0["hits"].sum() <= r["hits"].sum() <= big["hits"].sum()
+
+
+def test_cache_hand_sequence_with_aging():
+    """The aging branch: counts halved after every aging_period-th step change
+    which misses are admitted (hand-traced; the same trace without aging
+    admits nothing after step 0)."""
+    g = json.load(open(os.path.join(GOLDEN, "cache_sequence_aging.json")))
+    steps = len(g["access"])
+    acc = -np.ones((steps, 1, 2), np.int32)
+    for s, a in enumerate(g["access"]):
+        acc[s, 0, : len(a)] = a
+    r = oracle.cache_sim(g["L"], g["E"], g["C"], acc, aging_period=g["aging_period"])
+    assert r["hits"][:, 0].tolist() == g["hits"]
+    assert r["misses"][:, 0].tolist() == g["misses"]
+    assert r["admissions"] == g["admissions"] and r["evictions"] == g["evictions"]
+    assert r["slot_owner"].tolist() == g["slot_owner"]
+    w = g["without_aging"]
+    r0 = oracle.cache_sim(g["L"], g["E"], g["C"], acc, aging_period=0)
+    assert r0["hits"][:, 0].tolist() == w["hits"] and r0["misses"][:, 0].tolist() == w["misses"]
+    assert r0["admissions"] == w["admissions"] and r0["evictions"] == w["evictions"]
+    assert r0["slot_owner"].tolist() == w["slot_owner"]
+
+
+def test_cache_aging_special_cases():
+    """aging_period longer than the run is no aging; aging_period 1 halves
+    after every step, so with per-step counts of at most 1 every count is 0
+    at each step's end and an incumbent is replaced by any miss it is
+    evictable against (1 > 0)."""
+    L, E, steps, d = 2, 30, 40, 4
+    acc = _random_access(L, E, steps, d, 9)
+    base = oracle.cache_sim(L, E, 11, acc)
+    long = oracle.cache_sim(L, E, 11, acc, aging_period=steps + 1)
+    for key in ("hits", "misses", "slot_owner"):
+        np.testing.assert_array_equal(base[key], long[key])
+    assert base["admissions"] == long["admissions"] and base["evictions"] == long["evictions"]
+    one = oracle.cache_sim(L, E, 11, acc, aging_period=1)
+    # (a step has L*d = 8 accesses, so at least 11 - 8 + 1 residents stay evictable)
+    total_miss = int(one["misses"].sum())
+    assert one["admissions"] == total_miss
+    assert one["hits"].sum() + total_miss == (acc >= 0).sum()
