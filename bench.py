@@ -237,27 +237,73 @@ def replica_value(tokens_per_rank_step: int, ws: int, ms_step: float) -> float:
     return ws * tokens_per_rank_step / (ms_step * 1e-3)
 
 
-def cpu_baseline(wl, tokens: int = 3, seed_base: int = 77):
-    """The oracle (single-threaded C, fp64 FFN) on `tokens` single-token
-    forwards of the workload: routing over the layer, then the routed experts
-    quantised, dequantised and evaluated.  Returns (tokens/s, seconds, sample)."""
+_CPU_SAMPLES = {}
+
+
+def _cpu_sample(wl, tokens: int, seed_base: int):
+    """Inputs of the CPU baseline, made before any timing: `tokens`
+    single-token layer inputs and, quantised by the oracle, the experts they
+    are routed to (quantisation is the placement step, not the forward)."""
+    key_ = (wl.name, tokens, seed_base)
+    if key_ in _CPU_SAMPLES:
+        return _CPU_SAMPLES[key_]
+    import concurrent.futures as cf
     import oracle
     from synth import workloads as W
     wr, bias, _ = W.router(wl, 0)
-    t0 = time.perf_counter()
-    for i in range(tokens):
-        x = W.tokens(wl, seed_base + i, 0, 1)
-        lg = oracle.router_logits(x, wr, bias)
-        idx, _ = oracle.topk(lg, wl.top_k)
-        experts = [None] * wl.experts
-        for e in np.unique(idx):
-            q = [oracle.quantize(W.expert_master(wl, 0, int(e), m), wl.bits, wl.group, wl.scale_dtype)
-                 for m in range(3)]
-            experts[int(e)] = oracle.QuantExpert([c for c, _ in q], [s for _, s in q])
+    xs = [W.tokens(wl, seed_base + i, 0, 1) for i in range(tokens)]
+    need = set()
+    for x in xs:
+        idx, _ = oracle.topk(oracle.router_logits(x, wr, bias), wl.top_k)
+        need |= set(int(e) for e in np.unique(idx))
+
+    def quant(e):
+        q = [oracle.quantize(W.expert_master(wl, 0, e, m), wl.bits, wl.group, wl.scale_dtype)
+             for m in range(3)]
+        return e, oracle.QuantExpert([c for c, _ in q], [s for _, s in q])
+
+    experts = [None] * wl.experts
+    with cf.ThreadPoolExecutor(max(1, os.cpu_count() or 1)) as ex:
+        for e, qe in ex.map(quant, sorted(need)):
+            experts[e] = qe
+    _CPU_SAMPLES[key_] = (wr, bias, xs, experts)
+    return _CPU_SAMPLES[key_]
+
+
+def cpu_baseline(wl, tokens: int, threads: int = 1, seed_base: int = 77):
+    """The oracle (plain C, fp32 router logits in the fixed order, fp64 FFN)
+    on `tokens` single-token forwards of the workload's layer -- routing over
+    all E experts, dequantisation and FFN of the routed experts, combine --
+    spread over `threads` host threads (one token per task; the oracle itself
+    is single-threaded).  Returns (tokens/s, seconds, sample description)."""
+    import concurrent.futures as cf
+    import oracle
+    wr, bias, xs, experts = _cpu_sample(wl, tokens, seed_base)
+
+    def one(x):
         oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
                                     wl.scale_dtype, x, wr, bias, [0])
+
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for x in xs:
+            one(x)
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, xs))
     dt = time.perf_counter() - t0
-    return tokens / dt, dt, f"{tokens} single-token forwards of the decode layer (routing + quantise + fp64 FFN of the routed experts)"
+    return tokens / dt, dt, (f"{tokens} single-token forwards of the decode layer on {threads} host "
+                             f"thread(s) (routing over all experts + dequantise + fp64 FFN of the routed "
+                             f"experts + combine; experts quantised beforehand, untimed)")
+
+
+def cpu_baselines(wl, seed_base: int = 77) -> dict:
+    """The oracle timed on the host at 1 thread and at os.cpu_count() threads."""
+    cores = os.cpu_count() or 1
+    v1, dt1, s1 = cpu_baseline(wl, 3, 1, seed_base)
+    vn, dtn, sn = cpu_baseline(wl, 2 * cores, cores, seed_base + 1000)
+    return {"value": vn, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sn,
+            "seconds": dtn, "single_thread": {"value": v1, "cores": 1, "sample": s1, "seconds": dt1}}
 
 
 DECODE_WORKLOAD = ("decode MoE layer: H=4096, I=1024, E=384, top-6, int3 G128 bf16 scales, Zipf(1.0), "
@@ -275,23 +321,21 @@ def run_reference(args):
     oracle.build()
     import synth
     synth.build()
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        cpu_baseline(wl, tokens=1, seed_base=10)
-    vals = []
+    cores = os.cpu_count() or 1
+    cpu_baseline(wl, cores, cores, seed_base=10)  # warm-up (also builds the sample's experts)
     total_tokens, total_s = 0, 0.0
-    for s in range(args.steps):
-        v, dt, sample = cpu_baseline(wl, tokens=1, seed_base=100 + s)
-        total_tokens += 1
+    for s in range(args.steps):  # each step: a bounded sample of `cores` tokens, one per thread
+        v, dt, sample = cpu_baseline(wl, cores, cores, seed_base=10)
+        total_tokens += cores
         total_s += dt
     value = total_tokens / total_s
     line = {"impl": "reference", "metric": "MoE decode tokens/s", "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": DECODE_WORKLOAD, "parallelism": "host CPU, 1 thread"},
-            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": 1,
-                             "sample": f"bounded sample of the workload: {args.steps} single-token forwards "
-                                       "(routing + quantise + fp64 FFN of the routed experts), one per step"},
+            "config": {"workload": DECODE_WORKLOAD, "parallelism": f"host CPU, {cores} threads"},
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": cores,
+                             "sample": f"bounded sample of the workload per step: {sample}"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -367,6 +411,7 @@ def run_ours(args):
     ck = clocks.stop()
     ms = [a.elapsed_time(b) for a, b in times]
     ms_step = float(np.mean(ms))
+    ms_median, ms_min = float(np.median(ms)), float(np.min(ms))
     st = plan.stats(0)
     fw = max(st["forwards"], 1)
     hbm_b = st["hbm_bytes"] / args.steps     # per step (3 forwards)
@@ -404,6 +449,8 @@ def run_ours(args):
                              "roofline_us": rt * 1e6, "roofline_frac": rt / (m * 1e-3),
                              "roofline_frac_max_form": rtm / (m * 1e-3)}
 
+    popularity = realised_popularity(plan, wl, info, dev, rank)
+
     # end to end through the host-buffer entry point (pinned buffers, copies timed)
     xh = {T: [xs[T][s].view(torch.int16).cpu().pin_memory() for s in range(4)] for T in BATCHES}
     yh = {T: torch.empty(T, H, dtype=torch.int16).pin_memory() for T in BATCHES}
@@ -424,14 +471,13 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        v, dt, sample = cpu_baseline(wl, tokens=args.cpu_tokens)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
-               "seconds": dt}
+        cpu = cpu_baselines(wl)
 
     if rank == 0:
         line = {
             "metric": "MoE decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_median": ms_median, "ms_per_step_min": ms_min,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; weights N(0,0.02) quantised by the library's GPU quantiser)",
             "config": {"workload": DECODE_WORKLOAD,
@@ -450,6 +496,7 @@ def run_ours(args):
                          "hbm_bytes_per_step": hbm_b, "host_bytes_per_step": host_b,
                          "frac_max_form": roof_max_s / (ms_step * 1e-3)},
             "per_batch": per_batch,
+            "popularity": popularity,
             "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
                      "gpu": _numa_node(local)},
             "e2e": {"value": ws * tokens_step / (e2e_step * 1e-3), "unit": "tokens/s",
@@ -458,10 +505,63 @@ def run_ours(args):
             "clocks": ck, "wall_s_timed": wall,
             "cpu_baseline": cpu,
         }
-        print(json.dumps(line), flush=True)
     plan.close()
+    if rank == 0 and not args.no_prefill:
+        # the prefill layer (tensor-core path) in the same run, as an extra key
+        pre = prefill_measure(args, steps=max(5, min(args.steps, 20)), warmup=3, cpu=not args.no_cpu)
+        line["prefill"] = pre
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def realised_popularity(plan, wl, info, dev, rank: int, batches: int = 512, T: int = 6) -> dict:
+    """Realised routing of the decode layer over `batches` fresh T-token
+    inputs (through the forward's routing outputs): per-expert slot counts
+    summarised against the Plackett-Luce Zipf(s) targets of the workload."""
+    import torch
+    from synth import popularity as P
+    from synth import workloads as W
+    H, E, k = wl.hidden, wl.experts, wl.top_k
+    idx = torch.empty(batches, T, k, dtype=torch.int32, device=dev)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    xs = torch.from_numpy(np.stack([W.tokens(wl, 90000 + 131 * rank + b, 0, T) for b in range(batches)])
+                          .view(np.int16)).to(dev).view(torch.bfloat16)
+    plan.stats(0, reset=True)
+    for b in range(batches):
+        plan.forward(0, xs[b], y, dbg=dict(topk_idx=idx[b]))
+    torch.cuda.synchronize()
+    st = plan.stats(0, reset=True)
+    sel = idx.cpu().numpy().reshape(-1, k)
+    _, _, rank_of = info["routers"][0]
+    host = np.zeros(E, bool)
+    host[list(info["host_sets"][0])] = True
+    counts = np.bincount(sel.ravel(), minlength=E)
+    by_rank = np.zeros(E, np.int64)
+    by_rank[rank_of] = counts
+    target = P.plackett_luce_inclusion(E, k, wl.zipf_s)
+    n_tok = sel.shape[0]
+    top = max(1, E // 100)
+    # Zipf exponent fitted to the realised inclusion rates of the top half of the ranks
+    r = np.arange(1, E // 2 + 1)
+    ok = by_rank[: E // 2] > 0
+    slope = float(np.polyfit(np.log(r[ok]), np.log(by_rank[: E // 2][ok] / n_tok), 1)[0]) if ok.sum() > 2 else None
+    tgt_slope = float(np.polyfit(np.log(r), np.log(target[: E // 2]), 1)[0])
+    n_host = int(host.sum())
+    return {
+        "tokens": int(n_tok), "forwards": batches, "T": T,
+        "host_share_of_slots": float(host[sel].mean()),
+        "host_share_target": float(target[E - n_host:].sum() / k),
+        "p_any_host_per_token": float(host[sel].any(axis=1).mean()),
+        "top1pct_share_of_slots": float(by_rank[:top].sum() / sel.size),
+        "top1pct_share_target": float(target[:top].sum() / k),
+        "loglog_slope_top_half": slope, "loglog_slope_target": tgt_slope,
+        "experts_never_routed": int((counts == 0).sum()),
+        "distinct_experts_per_forward": st["accesses"] / max(st["forwards"], 1),
+        "host_experts_per_forward": st["misses"] / max(st["forwards"], 1),
+        "note": "realised per-expert slot counts of the decode layer's router on fresh N(0,1) inputs, "
+                "against the Plackett-Luce Zipf(s) inclusion rates the synthetic router bias is calibrated to"}
 
 
 def _common_line(args, metric, value, unit, ms, config, extra):
@@ -677,9 +777,10 @@ def run_cached(args):
     plan.close()
 
 
-def run_prefill(args):
+def prefill_measure(args, steps: int, warmup: int, cpu: bool = True) -> dict:
     """Prefill layer (config "prefill"): T = 8192 tokens through one layer
-    (H=4096, I=1024, E=384, top-6, int4 G128 bf16 scales, all experts in HBM)."""
+    (H=4096, I=1024, E=384, top-6, int4 G128 bf16 scales, all experts in HBM).
+    Returns the measurement as a dict (the keys of a bench line)."""
     import torch
     from moe_expert_layer_sorted_gb300 import harness
     from synth import workloads as W
@@ -700,7 +801,7 @@ def run_prefill(args):
     y = torch.empty_like(xs[0])
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
-        for w in range(args.warmup):
+        for w in range(warmup):
             plan.forward(0, xs[w % pool], y, stream=stream)
     stream.synchronize()
     plan.stats(0, reset=True)
@@ -708,7 +809,7 @@ def run_prefill(args):
     clocks.start()
     ev = []
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
+        for i in range(steps):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -717,7 +818,8 @@ def run_prefill(args):
             ev.append((a, b))
     torch.cuda.synchronize()
     ck = clocks.stop()
-    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    all_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = float(np.mean(all_ms))
     flops_ffn = 6.0 * T * k * H * I
     flops_router = 2.0 * T * E * H
     achieved = (flops_ffn + flops_router) / (ms * 1e-3) / 1e12
@@ -727,7 +829,7 @@ def run_prefill(args):
     yh = torch.empty_like(xh).pin_memory()
     e2e = []
     with torch.cuda.stream(stream):
-        for i in range(max(2, args.steps // 2)):
+        for i in range(max(2, steps // 2)):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -736,24 +838,41 @@ def run_prefill(args):
             b.synchronize()
             e2e.append(a.elapsed_time(b))
     e2e_ms = float(np.mean(e2e))
-    line = _common_line(
-        args, "MoE prefill tokens/s", T / (ms * 1e-3), "tokens/s", ms,
-        {"workload": wl.desc, "tokens_per_step": T,
-         "l2": "no flush: a step streams ~2.5 GB of weights, far above L2", "cuda_graph": False,
-         "parallelism": "single GPU"},
-        {"tflops": achieved,
-         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                      "frac": achieved / tpeak, "traffic": _recorded_traffic("pf_gemm_kernel_prefill_T8192"),
-                      "traffic_note": "DRAM read+write bytes of one gate/up GEMM launch (the dominant kernel) from "
-                                      "the ncu summary in profiles/ (null when the kernel changed since)",
-                      "kernel": "whole prefill forward (router, grouping, tcgen05 gate/up and down GEMMs, combine)",
-                      "peak_note": f"dense bf16, {tkind} burst figure; FLOPs = 6*T*k*H*I (expert FFNs) + 2*T*E*H (router)"},
-         "cache": {k_: st[k_] for k_ in ("accesses", "hits", "hbm_bytes")},
-         "e2e": {"value": T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
-                 "d2h_bytes_per_step": T * H * 2},
-         "setup_s": build_s, "gpu_launches": 10 * args.steps, "clocks": ck})
-    print(json.dumps(line), flush=True)
     plan.close()
+    del xs, y
+    torch.cuda.empty_cache()
+    out = {
+        "metric": "MoE prefill tokens/s", "value": T / (ms * 1e-3), "unit": "tokens/s", "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "ms_per_step_median": float(np.median(all_ms)),
+        "ms_per_step_min": float(np.min(all_ms)), "dtype": "bf16",
+        "config": {"workload": wl.desc, "tokens_per_step": T,
+                   "l2": "no flush: a step streams ~2.5 GB of weights, far above L2", "cuda_graph": False},
+        "tflops": achieved,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": achieved / tpeak, "traffic": _recorded_traffic("pf_gemm_kernel_prefill_T8192"),
+                     "traffic_note": "DRAM read+write bytes of one gate/up GEMM launch (the dominant kernel) from "
+                                     "the ncu summary in profiles/ (null when the kernel changed since)",
+                     "kernel": "whole prefill forward (router, grouping, tcgen05 gate/up and down GEMMs, combine)",
+                     "peak_note": f"dense bf16, {tkind} burst figure; FLOPs = 6*T*k*H*I (expert FFNs) + 2*T*E*H (router)"},
+        "cache": {k_: st[k_] for k_ in ("accesses", "hits", "hbm_bytes")},
+        "e2e": {"value": T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2},
+        "setup_s": build_s, "gpu_launches": 10 * steps, "clocks": ck}
+    if cpu:
+        cores = os.cpu_count() or 1
+        v, dt, sample = cpu_baseline(wl, 2 * cores, cores, seed_base=600)
+        out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": sample.replace("decode layer", "prefill layer (int4)"), "seconds": dt}
+    return out
+
+
+def run_prefill(args):
+    m = prefill_measure(args, steps=args.steps, warmup=args.warmup, cpu=not args.no_cpu)
+    extra = {k_: v for k_, v in m.items() if k_ not in ("metric", "value", "unit", "ms_per_step", "config",
+                                                       "steps", "warmup", "dtype")}
+    line = _common_line(args, m["metric"], m["value"], m["unit"], m["ms_per_step"],
+                        dict(m["config"], parallelism="single GPU"), extra)
+    print(json.dumps(line), flush=True)
 
 
 def run_cpu_vs_uva(args):
@@ -991,7 +1110,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=3)
+    ap.add_argument("--no-prefill", action="store_true", help="decode: leave out the prefill key")
     ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
                                                               "cpu-vs-uva", "prefetch-bound",
                                                               "prefill-staging"])

@@ -190,7 +190,15 @@ moe_status moe_layer_forward_host(moe_plan* plan, int layer, const void* x_host,
 moe_status moe_step_end(moe_plan* plan, void* stream);
 
 /* Counters of `layer` (or of all layers for layer = -1); reset = 1 zeroes
- * them after reading.  Synchronises with the plan's device work. */
+ * them after reading.  Synchronises with the plan's device work.  The hit
+ * rate these counters give is the measure of "Running a 24k-expert MoE on a
+ * single 32 GB card", section 3 (a cache of ~70 % of the experts serving
+ * 97.8-99.7 % of expert reads).  Under LFU each step queues its misses for
+ * moe_step_end in a queue of num_layers * min(E, max_tokens * k) entries; a
+ * forward that finds it full (a layer forwarded more than once between step
+ * ends) latches the fact, and the next moe_layer_forward, moe_step_end or
+ * moe_cache_stats that sees it returns MOE_ERR_STATE (this call, which
+ * synchronises first, always sees it; *out is filled all the same). */
 moe_status moe_cache_stats(moe_plan* plan, int layer, moe_cache_stats_t* out, int reset);
 
 /* Residence of every expert of `layer` as seen by the next forward: out[e] =
@@ -225,11 +233,17 @@ moe_status moe_probe_bandwidth(int device, size_t bytes, int iters, double* host
  * to the lower expert index) to topk_idx [T][k] int32 and the renormalised
  * softmax weights to topk_w [T][k] fp32 (both device).  Work space for the
  * logits is a fixed device array of 262,144 floats (1 MiB) that every GPU
- * loading this library holds until the process exits; T * E above that is
- * rejected with MOE_ERR_INVALID, as are H not a positive multiple of 256,
- * k outside [1, min(E, 8)] and x or wr not 16-byte aligned.  The first call
- * on a device looks up that array's device address (cudaGetSymbolAddress)
- * with the device current; make that first call before any stream capture.
+ * holds from the moment this library's device code is loaded into its
+ * context until the process exits; T * E above that is rejected with
+ * MOE_ERR_INVALID, as are H not a positive multiple of 256, k outside
+ * [1, min(E, 8)], x or wr not 16-byte aligned, and a stream that belongs
+ * to another device than the current one.  The first call on a device looks
+ * up that array's device address (cudaGetSymbolAddress) with the device
+ * current; under CUDA's lazy module loading this is also where the array's
+ * memory is committed, so make that first call early (a call with T = 0 does
+ * it and nothing else) and before any stream capture.  Selection follows the
+ * same order as moe_layer_forward (an order-preserving integer key of each
+ * logit, -0 equal to +0; ties to the lower expert index).
  * All calls share the one array, so calls whose work overlaps on the GPU
  * (different streams, or different host threads) race and give wrong
  * results; order them on one stream.  Stream-ordered; T = 0 is a no-op.

@@ -243,9 +243,23 @@ def probe_bandwidth(device=0, nbytes=1 << 30, iters=5) -> tuple[float, float]:
 def route_noalloc(x, wr, bias, k, topk_idx, topk_w, stream=None):
     """Router logits + top-k without any allocation by the library (see
     moe_route_noalloc in include/moe.h): all buffers are the caller's device
-    tensors; work space is a fixed device array inside the library."""
+    tensors; work space is a fixed device array inside the library.
+    x [T][H] and wr [E][H] hold bf16 (bfloat16 or int16 bit patterns), bias
+    [E] float32 or None, topk_idx [T][k] int32 and topk_w [T][k] float32, all
+    contiguous and on one CUDA device."""
+    import torch
     T, H = x.shape
     E = wr.shape[0]
+    bf16_like = (torch.bfloat16, torch.int16)
+    assert x.is_cuda and x.is_contiguous() and x.dtype in bf16_like, "x: contiguous bf16 [T][H] on a GPU"
+    assert wr.is_contiguous() and wr.dtype in bf16_like and tuple(wr.shape) == (E, H), "wr: contiguous bf16 [E][H]"
+    assert topk_idx.is_contiguous() and topk_idx.dtype == torch.int32 and tuple(topk_idx.shape) == (T, k)
+    assert topk_w.is_contiguous() and topk_w.dtype == torch.float32 and tuple(topk_w.shape) == (T, k)
+    tensors = [x, wr, topk_idx, topk_w]
+    if bias is not None:
+        assert bias.is_contiguous() and bias.dtype == torch.float32 and tuple(bias.shape) == (E,)
+        tensors.append(bias)
+    assert all(t.device == x.device for t in tensors), "every buffer on the same device"
     rc = lib().moe_route_noalloc(_addr(x), T, H, _addr(wr), _addr(bias), E, k, _addr(topk_idx),
                                  _addr(topk_w), _stream(stream))
     if rc != MOE_OK:

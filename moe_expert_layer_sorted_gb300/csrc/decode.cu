@@ -657,6 +657,7 @@ expert_decode_kernel(ExpertArgs a) {
         if (d < R.nh) {
           const unsigned mi = atomicAdd(a.miss_count, 1u);
           if ((int)mi < a.miss_cap) a.miss_list[mi] = (int32_t)gid;
+          else *reinterpret_cast<volatile uint32_t*>(a.err + 1) = 1u;  // queue full: latched
         }
       }
     }

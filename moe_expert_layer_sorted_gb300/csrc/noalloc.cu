@@ -1,6 +1,9 @@
 // Routing that allocates nothing: router logits and top-k for callers that
-// cannot call cudaMalloc.  The logits live in a fixed device array that this
-// library reserves when it is loaded; see moe_route_noalloc in moe.h.
+// cannot call cudaMalloc.  The logits live in a fixed device array of this
+// library; its memory is committed in a CUDA context when the library's
+// module is loaded there (with lazy module loading, at this entry point's
+// first call on that device, which also looks up the array's address); see
+// moe_route_noalloc in moe.h.
 #include <mutex>
 
 #include "internal.h"
@@ -53,9 +56,18 @@ __global__ void noalloc_logits_kernel(const uint16_t* __restrict__ x, int T, int
   if (lane == 0) logits[wid] = acc + (bias ? bias[e] : 0.0f);
 }
 
-// Top-k of one token per warp: k rounds of a warp argmax over the token's
-// logits (logit descending, ties to the lower expert index), then the
-// softmax renormalised over the k chosen.
+// Order-preserving integer key of a logit (-0 folded to +0): larger float,
+// larger key; the same key the plan's forward paths select on.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k of one token per warp: k rounds, each taking every lane's best
+// untaken logit (largest key; lanes scan experts in ascending order, so the
+// lower index wins a tie within a lane), then the warp's largest key and,
+// among the lanes holding it, the lowest expert index (ties to the lower
+// index); then the softmax renormalised over the k chosen, summed in j order.
 __global__ void noalloc_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                     int32_t* __restrict__ idx, float* __restrict__ w) {
   const int lane = threadIdx.x & 31;
@@ -65,28 +77,22 @@ __global__ void noalloc_topk_kernel(const float* __restrict__ logits, int T, int
   int chosen[kMaxTopK];
   float cv[kMaxTopK];
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    uint32_t bk = 0u;  // below every real key
+    int bi = -1;
     for (int e = lane; e < E; e += 32) {
       bool taken = false;
       for (int q = 0; q < j; ++q) taken |= chosen[q] == e;
-      const float v = l[e];
-      if (!taken && (bi == 0x7fffffff || v > bv)) {  // e ascending: ties keep the lower index
-        bv = v;
+      const uint32_t key = logit_key(l[e]);
+      if (!taken && (bi < 0 || key > bk)) {
+        bk = key;
         bi = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    chosen[j] = bi;
-    cv[j] = bv;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+    const uint32_t mine = (bi >= 0 && bk == kmax) ? (uint32_t)bi : 0xffffffffu;
+    const int win = (int)__reduce_min_sync(0xffffffffu, mine);
+    chosen[j] = win;
+    cv[j] = l[win];
   }
   if (lane == 0) {
     float ex[kMaxTopK];
@@ -102,11 +108,11 @@ __global__ void noalloc_topk_kernel(const float* __restrict__ logits, int T, int
   }
 }
 
-
 }  // namespace
 
-// Address of the fixed array on the current device, looked up once per device.
-static moe_status scratch_for_current_device(float** out) {
+// Address of the fixed array on the current device, looked up once per device
+// (the lookup loads the module into the context if it is not yet loaded).
+static moe_status scratch_for_current_device(float** out, int* dev_out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -117,11 +123,13 @@ static moe_status scratch_for_current_device(float** out) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess || !p) {
+      cudaGetLastError();  // leave no error behind for the caller's next check
       return MOE_ERR_CUDA;
     }
     g_scratch[dev] = static_cast<float*>(p);
   }
   *out = g_scratch[dev];
+  *dev_out = dev;
   return MOE_OK;
 }
 
@@ -138,11 +146,19 @@ extern "C" moe_status moe_route_noalloc(const void* x_bf16, int T, int H, const 
   if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) || (reinterpret_cast<uintptr_t>(wr_bf16) & 15)) {
     return MOE_ERR_INVALID;
   }
-  if (T == 0) return MOE_OK;
+  // set-up first, so that a call with T = 0 can serve as the warm-up
   float* logits = nullptr;
-  const moe_status st = scratch_for_current_device(&logits);
+  int dev = -1;
+  const moe_status st = scratch_for_current_device(&logits, &dev);
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int sdev = -1;  // the array's address is per device: the stream must be the current device's
+  if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_INVALID;
+  }
+  if (sdev != dev) return MOE_ERR_INVALID;
+  if (T == 0) return MOE_OK;
   const int64_t warps = (int64_t)T * E;
   noalloc_logits_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
       static_cast<const uint16_t*>(x_bf16), T, H, static_cast<const uint16_t*>(wr_bf16), bias, E,

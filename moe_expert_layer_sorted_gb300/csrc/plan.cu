@@ -58,6 +58,18 @@ struct Busy {
   }
 };
 
+// Word 1 of the mapped error page: set by a forward whose step's miss queue
+// was already full (its miss is not queued for the step-end admission pass).
+// Taken (read and cleared) by the next call that looks.
+constexpr const char* kOverflowMsg =
+    "an earlier forward found this step's miss queue full (a layer forwarded more than once "
+    "between step ends?); its misses were not queued for admission";
+bool take_overflow(Plan* p) {
+  if (!p->err_host || !p->err_host[1]) return false;
+  p->err_host[1] = 0;
+  return true;
+}
+
 bool is_device_ptr(const void* ptr) {
   if (!ptr) return false;
   cudaPointerAttributes a;
@@ -740,6 +752,7 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
     cudaDeviceSynchronize();
     return fail(p, MOE_ERR_TIMEOUT, "a bounded device-side wait of an earlier forward gave up");
   }
+  if (take_overflow(p)) return fail(p, MOE_ERR_STATE, kOverflowMsg);
   cudaStream_t s = (cudaStream_t)stream;
   if (p->have_last && p->last_stream != s) CK(p, cudaStreamWaitEvent(s, p->ev_done, 0));
   cudaError_t e;
@@ -782,6 +795,8 @@ extern "C" moe_status moe_step_end(moe_plan* plan, void* stream) {
     if (e != cudaSuccess) return cuda_fail(p, e, "step end");
   }
   p->step += 1;
+  // the step end ran (on the queued misses); an overflow seen by now is reported
+  if (take_overflow(p)) return fail(p, MOE_ERR_STATE, kOverflowMsg);
   return MOE_OK;
 }
 
@@ -796,6 +811,7 @@ extern "C" moe_status moe_cache_stats(moe_plan* plan, int layer, moe_cache_stats
   std::vector<unsigned long long> h((size_t)L * kNumStats);
   CK(p, cudaDeviceSynchronize());
   CK(p, cudaMemcpy(h.data(), p->stats, h.size() * 8, cudaMemcpyDeviceToHost));
+  const bool overflow = take_overflow(p);
   uint64_t acc[kNumStats] = {0};
   for (int l = 0; l < L; ++l)
     if (layer < 0 || l == layer)
@@ -815,6 +831,7 @@ extern "C" moe_status moe_cache_stats(moe_plan* plan, int layer, moe_cache_stats
     else CK(p, cudaMemset(p->stats + (size_t)layer * kNumStats, 0, kNumStats * 8));
     CK(p, cudaDeviceSynchronize());
   }
+  if (overflow) return fail(p, MOE_ERR_STATE, kOverflowMsg);  // *out is filled all the same
   return MOE_OK;
 }
 

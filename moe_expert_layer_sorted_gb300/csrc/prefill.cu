@@ -900,7 +900,8 @@ __global__ void pf_combine_kernel(const uint16_t* __restrict__ o, const int32_t*
 __global__ void pf_stats_kernel(const int32_t* __restrict__ counts, int E, const uint8_t* const* blob_hbm,
                                 unsigned long long* stats, int64_t expert_bytes, int64_t router_bytes,
                                 int n_pairs, int lfu, int64_t ge0, uint32_t* lfu_count, int32_t* lfu_last,
-                                const int* step, int32_t* miss_list, unsigned* miss_count, int miss_cap) {
+                                const int* step, int32_t* miss_list, unsigned* miss_count, int miss_cap,
+                                uint32_t* overflow) {
   __shared__ int sh[2];
   if (threadIdx.x == 0) sh[0] = sh[1] = 0;
   __syncthreads();
@@ -915,6 +916,7 @@ __global__ void pf_stats_kernel(const int32_t* __restrict__ counts, int E, const
       if (!hit) {
         const unsigned mi = atomicAdd(miss_count, 1u);
         if ((int)mi < miss_cap) miss_list[mi] = (int32_t)(ge0 + e);
+        else *reinterpret_cast<volatile uint32_t*>(overflow) = 1u;  // queue full: latched
       }
     }
   }
@@ -1090,7 +1092,8 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, p.blob_hbm + ge0, p.stats + (int64_t)layer * kNumStats,
                                     p.lay.algo_bytes, (int64_t)E * H * 2, n,
                                     d.cache_policy == MOE_POLICY_LFU, ge0, p.lfu_count, p.lfu_last,
-                                    &p.ctl->step, p.miss_list, p.miss_count, d.num_layers * p.max_distinct);
+                                    &p.ctl->step, p.miss_list, p.miss_count, d.num_layers * p.max_distinct,
+                                    p.err_dev + 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (dbg) {  // optional routing outputs
     if (dbg->logits) cudaMemcpyAsync(dbg->logits, p.logits, (size_t)T * E * 4, cudaMemcpyDeviceToDevice, s);

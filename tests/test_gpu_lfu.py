@@ -112,3 +112,97 @@ def test_lfu_admission_counters():
 def plan_expert_bytes(wl):
     return sum(wl.codes_bytes(m) + wl.matrix_shape(m)[0] * (wl.matrix_shape(m)[1] // wl.group) * 2
                for m in range(3))
+
+
+# The cached-decode cache at its full size: 48 layers x 512 experts, 17,203
+# HBM slots (70 %), so the device's victim scan walks every slot in several
+# rounds per thread; counts halved every 16 steps; eight tokens per step so
+# that the run touches more experts than the cache holds and evicts.  The
+# expert matrices keep the cached workload's shape (H=2048, I=512, int2 G64
+# fp16 scales): the cache rules do not depend on it, the bytes do.
+WL_FULL = W.Workload("lfu-full", 48, 512, 2048, 512, 8, (8,), 2, 64, W.SC_F16, "zipf", 1.2,
+                     cache_frac=0.7, steps=320, drift=0.01)
+AGING = 16
+
+
+def test_lfu_full_size_with_aging_matches_cache_simulator():
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    wl = WL_FULL
+    plan, info = harness.build_plan(wl, gpu_gen=True, aging_period=AGING)
+    C = plan.desc.cache_slots
+    assert C == 17_203
+    L, E, k, T, S = wl.layers, wl.experts, wl.top_k, 8, wl.steps
+    idx_all = torch.empty(S, L, T, k, dtype=torch.int32, device="cuda")
+    xs = torch.empty(S, L, T, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    import synth
+    cs = torch.cuda.current_stream().cuda_stream
+    for s in range(S):
+        for l in range(L):
+            synth.normal_bf16_device(W.key(wl.seed, W.TAG_X, s, l), T * wl.hidden, 1.0,
+                                     xs[s, l].data_ptr(), cs)
+    y = torch.empty(T, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    biases = np.stack([info["routers"][l][1] for l in range(L)]).astype(np.float32)
+    hits = np.zeros((S, L), np.int64)
+    misses = np.zeros((S, L), np.int64)
+    plan.stats(-1, reset=True)
+    for s in range(S):
+        for l in range(L):
+            plan.forward(l, xs[s, l], y, dbg=dict(topk_idx=idx_all[s, l]))
+        for l in range(L):
+            st = plan.stats(l, reset=True)
+            hits[s, l], misses[s, l] = st["hits"], st["misses"]
+        plan.step_end()
+        biases = biases + np.stack([W.bias_drift(wl, s, l) for l in range(L)])
+        plan.update_router_biases(0, np.ascontiguousarray(biases, dtype=np.float32))
+    torch.cuda.synchronize()
+    idx = idx_all.cpu().numpy()
+    maxd = T * k
+    access = np.full((S, L, maxd), -1, np.int32)
+    for s in range(S):
+        for l in range(L):
+            d = np.unique(idx[s, l])
+            access[s, l, : len(d)] = d
+    sim = oracle.cache_sim(L, E, C, access, aging_period=AGING)
+    tot = plan.stats(-1)
+    slot_of = np.concatenate([plan.residence(l) for l in range(L)])
+    plan.close()
+    assert sim["evictions"] > 1000, sim["evictions"]  # the cache filled and kept turning over
+    np.testing.assert_array_equal(hits, sim["hits"])
+    np.testing.assert_array_equal(misses, sim["misses"])
+    assert tot["admissions"] == sim["admissions"] and tot["evictions"] == sim["evictions"]
+    owner = np.full(C, -1, np.int64)
+    for g, c in enumerate(slot_of):
+        if c >= 0:
+            assert owner[c] == -1
+            owner[c] = g
+    np.testing.assert_array_equal(owner, sim["slot_owner"])
+
+
+def test_lfu_miss_queue_overflow_is_reported():
+    """Forwarding one layer more often between step ends than the step's
+    miss queue allows (here: 3 forwards of a one-layer plan with a queue of
+    min(E, T*k) misses) latches the overflow; the next call that looks
+    reports MOE_ERR_STATE once, and the plan then works as before."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import MoeError, harness
+    wl = W.Workload("lfu-overflow", 1, 64, 256, 128, 4, (4,), 2, 64, W.SC_F16, "plain",
+                    cache_frac=0.1, steps=1)
+    plan, _ = harness.build_plan(wl)
+    T = 4
+    y = torch.empty(T, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    for s in range(3):
+        plan.forward(0, _xw(wl, s, T), y)
+    with pytest.raises(MoeError) as ei:
+        plan.stats(0)
+    assert ei.value.status == 5 and "miss queue" in str(ei.value)
+    plan.step_end()
+    plan.forward(0, _xw(wl, 9, T), y)
+    st = plan.stats(0)  # one forward per step again: no overflow
+    assert st["forwards"] == 4
+    plan.close()
+
+
+def _xw(wl, step, T):
+    import torch
+    return torch.from_numpy(W.tokens(wl, step, 0, T).view(np.int16).copy()).cuda().view(torch.bfloat16)

@@ -330,3 +330,38 @@ def test_bounded_wait_runs_out_and_the_plan_recovers():
         y2, _ = _run(plan, 0, x, wl)
         assert torch.equal(y2.view(torch.int16), y0.view(torch.int16))
     plan.close()
+
+
+def _shifted_tokens(wl, seed, T, mode):
+    """Layer inputs at the method's numerical edge: a large common offset
+    (c + N(0,1), c = 8 or 64), or N(0,1) with eight outlier columns of
+    +-1000 (every column of a token offset or outlying, so the integer-code
+    zero-point sums of every scale group carry it)."""
+    x = oracle.bf16_to_f32(W.tokens(wl, seed, 0, T)).astype(np.float32)
+    if mode.startswith("offset"):
+        x = x + np.float32(int(mode[6:]))
+    else:
+        cols = np.random.default_rng(seed).choice(wl.hidden, 8, replace=False)
+        x[:, cols] = np.where(np.arange(8) % 2 == 0, 1000.0, -1000.0).astype(np.float32)
+    return oracle.f32_to_bf16(x)
+
+
+@pytest.mark.parametrize("T", [1, 6])
+@pytest.mark.parametrize("mode", ["offset8", "offset64", "outliers"])
+def test_decode_activation_edge_cases(decode_layer, T, mode):
+    """Decode layer at full size with offset or outlying activations: routing
+    bit-exact, outputs within the per-token tolerance (the code offset folded
+    into per-group sums of x must not cancel catastrophically)."""
+    wl, plan, info = decode_layer
+    wr, bias, _ = info["routers"][0]
+    x = _shifted_tokens(wl, 7000 + T, T, mode)
+    y, r = _run(plan, 0, x, wl)
+    lg = oracle.router_logits(x, wr, bias)
+    idx, w = oracle.topk(lg, wl.top_k)
+    assert np.array_equal(r["logits"], lg)
+    assert np.array_equal(r["topk_idx"], idx)
+    np.testing.assert_allclose(r["topk_w"], w, rtol=2e-6, atol=1e-7)
+    experts = [_oracle_expert(wl, 0, e) if e in np.unique(idx) else None for e in range(wl.experts)]
+    ref = oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                                      wl.scale_dtype, x, wr, bias, np.arange(T))
+    assert _rel_err(_bf16_bits_to_f64(y), ref) <= TOL

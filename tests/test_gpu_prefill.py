@@ -210,3 +210,29 @@ def test_prefill_hidden_17_blocks():
     assert np.array_equal(r["perm"], ref["perm"])
     assert _rel_err(y, ref["y"]) <= TOL
     plan.close()
+
+
+@pytest.mark.parametrize("mode", ["offset8", "offset64", "outliers"])
+def test_prefill_activation_edge_cases(mode):
+    """Prefill with offset or outlying activations (c + N(0,1), or +-1000 in
+    eight columns): routing bit-exact, outputs within tolerance."""
+    from moe_expert_layer_sorted_gb300 import harness
+    wl, T = MID3, 300
+    plan, info = harness.build_plan(wl, max_tokens=T)
+    wr, bias, _ = info["routers"][0]
+    experts = [_oracle_expert(wl, 0, e) for e in range(wl.experts)]
+    x = oracle.bf16_to_f32(W.tokens(wl, 8100, 0, T)).astype(np.float32)
+    if mode.startswith("offset"):
+        x = x + np.float32(int(mode[6:]))
+    else:
+        cols = np.random.default_rng(5).choice(wl.hidden, 8, replace=False)
+        x[:, cols] = np.where(np.arange(8) % 2 == 0, 1000.0, -1000.0).astype(np.float32)
+    x = oracle.f32_to_bf16(x)
+    y, r = _run(plan, x, wl)
+    ref = oracle.layer_forward(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
+                               wl.scale_dtype, x, wr, bias)
+    assert np.array_equal(r["logits"], ref["logits"])
+    assert np.array_equal(r["topk_idx"], ref["idx"])
+    assert np.array_equal(r["perm"], ref["perm"])
+    assert _rel_err(y, ref["y"]) <= TOL
+    plan.close()
