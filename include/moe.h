@@ -246,7 +246,8 @@ moe_status moe_probe_bandwidth(int device, size_t bytes, int iters, double* host
  * logit, -0 equal to +0; ties to the lower expert index).
  * All calls share the one array, so calls whose work overlaps on the GPU
  * (different streams, or different host threads) race and give wrong
- * results; order them on one stream.  Stream-ordered; T = 0 is a no-op.
+ * results; order them on one stream.  Stream-ordered; T = 0 does the
+ * set-up only (its buffer pointers may be NULL).
  * Calls no allocator (no cudaMalloc, cudaFree or library allocation). */
 moe_status moe_route_noalloc(const void* x_bf16, int T, int H, const void* wr_bf16,
                              const float* bias, int E, int k, int32_t* topk_idx, float* topk_w,

@@ -193,10 +193,8 @@ cudaError_t moe::lfu_step_end(Plan& p, cudaStream_t s) {
   a.stats = p.stats;
   const size_t smem = (size_t)a.miss_cap * 4;
   cudaError_t e = cudaSuccess;
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(lfu_decide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  if (smem > 48 * 1024 && (e = ensure_dynamic_smem((const void*)lfu_decide_kernel, smem)) != cudaSuccess)
+    return e;
   lfu_decide_kernel<<<1, kDecideThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

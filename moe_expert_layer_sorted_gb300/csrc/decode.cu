@@ -67,6 +67,10 @@ namespace {
 constexpr int kRouterWarps = 4;
 constexpr int kMaxRing = 8;                             // cp.async ring depth bound, in units
 constexpr int kHostCtasMin = 4, kHostCtasMax = 16;  // CTAs given the host-resident experts' work
+// Work-time weight of a host-resident expert's units against an HBM one's when
+// the grid is split: a CTA reads pinned host memory over the link several
+// times slower than it streams and computes a unit from HBM.
+constexpr int kHostCost = 1;
 constexpr int kMaxSlots = kDecodeMaxTokens * kMaxTopK;  // (token, expert) pairs per forward
 
 // ------------------------------------------------------------------ router
@@ -697,9 +701,12 @@ expert_decode_kernel(ExpertArgs a) {
   // runs before anything it could be blocked by.
   const int nh = R.nh;
   int Ch = 0;
-  if (nh > 0 && nh < D && gridDim.x >= 2)  // the host share of the grid, within [4, 16] (4 fill the link)
-    Ch = min(min(kHostCtasMax, max(kHostCtasMin, ((int)gridDim.x * nh + D / 2) / D)),
+  if (nh > 0 && nh < D && gridDim.x >= 2) {  // the host share of the grid: the host units' share
+                                             // of the work time, within [kHostCtasMin, kHostCtasMax]
+    const int wh = kHostCost * nh, wt = wh + (D - nh);
+    Ch = min(min(kHostCtasMax, max(kHostCtasMin, ((int)gridDim.x * wh + wt / 2) / wt)),
              min(nh * (tilesI + nB), (int)gridDim.x / 2));
+  }
   const bool hostcta = (int)blockIdx.x < Ch;
   const int dlo = (Ch == 0 || hostcta) ? 0 : nh;
   const int dn = Ch == 0 ? D : (hostcta ? nh : D - nh);
@@ -1053,17 +1060,8 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
     const void* kfn = b == 2   ? (const void*)expert_decode_kernel<2>
                       : b == 3 ? (const void*)expert_decode_kernel<3>
                                : (const void*)expert_decode_kernel<4>;
-    if (cf.smem > p.dsmem_set) {  // only ever raised: a larger batch may already rely on it
-      e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cf.smem);
-      if (e != cudaSuccess) return e;
-      p.dsmem_set = cf.smem;
-    }
-    if (cf.rsmem > p.rsmem_set) {
-      e = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)cf.rsmem);
-      if (e != cudaSuccess) return e;
-      p.rsmem_set = cf.rsmem;
-    }
+    if ((e = ensure_dynamic_smem(kfn, cf.smem)) != cudaSuccess) return e;
+    if ((e = ensure_dynamic_smem((const void*)router_logits_kernel, cf.rsmem)) != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, (kWarps + 1) * 32, cf.smem);
     if (e != cudaSuccess) return e;

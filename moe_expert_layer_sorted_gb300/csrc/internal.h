@@ -147,13 +147,18 @@ struct Plan {
     size_t smem = 0, rsmem = 0;
     int grid = 0, slot_bytes = 0, nslots = 0;
   } dcfg[kDecodeMaxTokens + 1];
-  size_t dsmem_set = 0, rsmem_set = 0;  // largest max-dynamic-smem attributes set so far
 
   bool fail_next = false;  // test hook: the next decode forward publishes no gate/up results
 
   std::atomic<int> busy{0};
   std::string last_error;
 };
+
+// Makes `fn` launchable with `bytes` of dynamic shared memory on the current
+// device.  The attribute belongs to the function, not to a plan, so it is only
+// ever raised (process-wide, per device): lowering it for one plan would make
+// another plan's larger launch of the same kernel fail.
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
 // Launchers implemented in the .cu files (return cudaError_t of the launch).
 cudaError_t launch_repack(const uint8_t* src_codes, const void* src_scales, uint8_t* dst_blob,

@@ -136,14 +136,17 @@ static moe_status scratch_for_current_device(float** out, int* dev_out) {
 extern "C" moe_status moe_route_noalloc(const void* x_bf16, int T, int H, const void* wr_bf16,
                                         const float* bias, int E, int k, int32_t* topk_idx,
                                         float* topk_w, void* stream) {
-  if (!x_bf16 || !wr_bf16 || !topk_idx || !topk_w || T < 0 || H < 256 || H % 256 || E < 1 ||
-      k < 1 || k > kMaxTopK || k > E) {
+  if (T < 0 || H < 256 || H % 256 || E < 1 || k < 1 || k > kMaxTopK || k > E) {
     return MOE_ERR_INVALID;
   }
   if ((int64_t)T * E > kNoAllocMaxLogits) {
     return MOE_ERR_INVALID;
   }
-  if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) || (reinterpret_cast<uintptr_t>(wr_bf16) & 15)) {
+  // buffers are only read or written when there are tokens (T = 0 may pass NULL)
+  if (T > 0 && (!x_bf16 || !wr_bf16 || !topk_idx || !topk_w)) {
+    return MOE_ERR_INVALID;
+  }
+  if (T > 0 && ((reinterpret_cast<uintptr_t>(x_bf16) & 15) || (reinterpret_cast<uintptr_t>(wr_bf16) & 15))) {
     return MOE_ERR_INVALID;
   }
   // set-up first, so that a call with T = 0 can serve as the warm-up

@@ -6,6 +6,8 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 #include <new>
 
 #include "internal.h"
@@ -235,6 +237,20 @@ __global__ void read_probe_kernel(const uint4* __restrict__ p, int64_t n16, unsi
 }
 
 }  // namespace
+
+cudaError_t moe::ensure_dynamic_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> set;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& cur = set[{dev, fn}];
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
 
 // --------------------------------------------------------------- layout
 

@@ -938,7 +938,7 @@ cudaError_t launch_gemm(int bits, const CUtensorMap& map, const GemmArgs& a, int
   const void* fn = bits == 2   ? (const void*)pf_gemm_kernel<2, GATEUP>
                    : bits == 3 ? (const void*)pf_gemm_kernel<3, GATEUP>
                                : (const void*)pf_gemm_kernel<4, GATEUP>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return e;
   switch (bits) {
     case 2: pf_gemm_kernel<2, GATEUP><<<grid, kGemmThreads, smem, s>>>(map, a); break;
@@ -1015,9 +1015,7 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   cudaError_t e;
   {
     const dim3 grid((T + kRtTok - 1) / kRtTok, (E + kRtExp - 1) / kRtExp);
-    if ((e = cudaFuncSetAttribute(pf_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem)) !=
-        cudaSuccess)
-      return e;
+    if ((e = ensure_dynamic_smem((const void*)pf_router_kernel, kRtSmem)) != cudaSuccess) return e;
     pf_router_kernel<<<grid, 256, kRtSmem, s>>>(x, T, H, p.wr[layer], p.bias[layer], E, p.logits);
   }
   pf_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(p.logits, T, E, k, p.topk_idx, p.topk_w);
@@ -1025,7 +1023,7 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     const int nb = (n + kGroupChunk - 1) / kGroupChunk;
     const size_t hsm = (size_t)E * 4, wsm = (size_t)8 * E * 4;
     if (wsm > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(pf_bucket_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm)) != cudaSuccess)
+        (e = ensure_dynamic_smem((const void*)pf_bucket_place, wsm)) != cudaSuccess)
       return e;
     pf_bucket_count<<<nb, 256, hsm, s>>>(p.topk_idx, n, E, p.pf_bucket);
     pf_bucket_scan<<<1, 1024, 0, s>>>(p.pf_bucket, E, nb, p.counts, p.offsets);

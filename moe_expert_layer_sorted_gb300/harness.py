@@ -55,10 +55,11 @@ def build_plan(wl: W.Workload, *, max_tokens: int | None = None, layers: int | N
                host_overlap: int = 0, device: int = 0, all_hbm: bool = False, progress=None,
                gpu_gen: bool = False, aging_period: int = 0):
     """Create a plan for `wl` (first `layers` layers), set its routers and place
-    every expert (host-resident ones per the workload).  Returns (plan, info)."""
+    every expert (host-resident ones per the workload; with all_hbm, a static
+    plan with every expert in HBM).  Returns (plan, info)."""
     L = wl.layers if layers is None else layers
     T = max(wl.tokens) if max_tokens is None else max_tokens
-    lfu = wl.cache_frac > 0
+    lfu = wl.cache_frac > 0 and not all_hbm  # all_hbm: every expert in HBM, no cache
     host_sets = []
     routers = []
     for l in range(L):
