@@ -11,7 +11,7 @@ weight-stream GB/s against the HBM + host-link roofline.
 
 Prints one JSON line.  Timing: CUDA events on the launching stream around
 each step (the step's forwards are one CUDA-graph replay); L2 is flushed
-(256 MiB write) between steps, outside the timed events.  `--impl reference`
+(256 MiB written, then 256 MiB read) between steps, outside the timed events.  `--impl reference`
 times the CPU oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -101,6 +101,22 @@ def _tensor_peak():
             return float(json.load(f)["bf16_tflops"]), "measured"
     except Exception:
         return 1900.0, "fallback"
+
+
+class L2Flush:
+    """Between timed steps: write 256 MiB (more than the 126 MB L2), then read
+    another 256 MiB, so that L2 holds none of the step's weights and only
+    clean lines (a write alone would leave ~126 MB of dirty lines whose
+    write-back the next timed step would pay)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 class ClockSampler:
@@ -361,7 +377,7 @@ def run_ours(args):
     xs = {T: [torch.from_numpy(W.tokens(wl, 5000 + 97 * rank + s, 0, T).view(np.int16).copy())
               .to(dev).view(torch.bfloat16) for s in range(pool)] for T in BATCHES}
     ys = {T: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for T in BATCHES}
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     with torch.cuda.stream(stream):
         for T in BATCHES:  # first use sets the per-T launch configuration
@@ -386,7 +402,7 @@ def run_ours(args):
 
     with torch.cuda.stream(stream):
         for w in range(args.warmup):
-            flush.zero_()
+            flush()
             step(w)
     stream.synchronize()
     plan.stats(0, reset=True)
@@ -399,7 +415,7 @@ def run_ours(args):
     t_wall = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -431,7 +447,7 @@ def run_ours(args):
         tt = []
         with torch.cuda.stream(stream):
             for i in range(16):
-                flush.zero_()
+                flush()
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -457,7 +473,7 @@ def run_ours(args):
     e2e_ms = []
     with torch.cuda.stream(stream):
         for i in range(max(args.steps // 2, 4)):
-            flush.zero_()
+            flush()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -481,7 +497,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; weights N(0,0.02) quantised by the library's GPU quantiser)",
             "config": {"workload": DECODE_WORKLOAD,
-                       "tokens_per_step": tokens_step, "l2": "256 MiB flush between steps, outside the timed events",
+                       "tokens_per_step": tokens_step, "l2": "256 MiB written then 256 MiB read between steps, outside the timed events",
                        "cuda_graph": use_graph, "parallelism": "replicas" if ws > 1 else "single GPU"},
             "weight_stream_GBps": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": eff_peak, "unit": "GB/s",
@@ -903,7 +919,7 @@ def run_cpu_vs_uva(args):
             picks.append((xb, x, hs[0]))
         if len(picks) == args.cpu_vs_uva_picks:
             break
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush("cuda")
     stream = torch.cuda.Stream()
 
     def fwd_us(p, x):
@@ -917,7 +933,7 @@ def run_cpu_vs_uva(args):
         ev = []
         with torch.cuda.stream(stream):  # queued back to back: no idle gaps between the forwards
             for i in range(args.warmup + args.steps):
-                flush.zero_()
+                flush()
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -951,7 +967,7 @@ def run_cpu_vs_uva(args):
         args, "host-resident expert: GPU in-place read vs CPU compute (extra us per forward)", extra_us, "us",
         med("gpu_forward_us_with_host_expert") / 1e3,
         {"workload": wl.desc + "; T = 1 tokens routed to exactly one host-resident expert",
-         "l2": "256 MiB flush before each timed forward", "cuda_graph": True, "parallelism": "single GPU"},
+         "l2": "256 MiB written then 256 MiB read before each timed forward", "cuda_graph": True, "parallelism": "single GPU"},
         {"higher_is_better": False,
          "expert_bytes": 4915200, "link_GBps": link_gbs, "link_time_us": 4915200 / (link_gbs * 1e3),
          "gpu_forward_us_with_host_expert": med("gpu_forward_us_with_host_expert"),

@@ -84,8 +84,8 @@ typedef struct moe_plan_desc {
   int64_t hbm_experts;  /* STATIC: capacity of the HBM expert arena, in experts (the rest of
                            the L*E experts must be placed in host memory) */
   int64_t cache_slots;  /* LFU: number of HBM slots (0 = no cache: every read goes to host) */
-  int32_t host_overlap; /* 0: host- and HBM-resident experts are processed by one grid, host
-                           work first; 1: host-resident experts run on a second stream */
+  int32_t reserved0;    /* must be zero (host- and HBM-resident experts are always processed
+                           by one grid, with a share of its CTAs given to the host experts) */
   int32_t aging_period; /* LFU: halve all access counts every aging_period steps (0 = never) */
   int64_t reserved[4];  /* must be zero */
 } moe_plan_desc;

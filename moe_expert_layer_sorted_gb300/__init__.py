@@ -47,7 +47,7 @@ class PlanDesc(ctypes.Structure):
                 ("scale_dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("cache_policy", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("hbm_experts", ctypes.c_int64), ("cache_slots", ctypes.c_int64),
-                ("host_overlap", ctypes.c_int32), ("aging_period", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32), ("aging_period", ctypes.c_int32),
                 ("reserved", ctypes.c_int64 * 4)]
 
 
@@ -140,14 +140,14 @@ class Plan:
 
     def __init__(self, *, num_layers, num_experts, hidden, inter, top_k, weight_bits, group_size,
                  scale_dtype, max_tokens, cache_policy=POLICY_STATIC, hbm_experts=0,
-                 cache_slots=0, host_overlap=0, aging_period=0, device=0):
+                 cache_slots=0, aging_period=0, device=0):
         d = PlanDesc()
         d.struct_size = ctypes.sizeof(PlanDesc)
         d.num_layers, d.num_experts, d.hidden, d.inter = num_layers, num_experts, hidden, inter
         d.top_k, d.weight_bits, d.group_size, d.scale_dtype = top_k, weight_bits, group_size, scale_dtype
         d.max_tokens, d.cache_policy, d.device = max_tokens, cache_policy, device
         d.hbm_experts, d.cache_slots = hbm_experts, cache_slots
-        d.host_overlap, d.aging_period = host_overlap, aging_period
+        d.aging_period = aging_period
         self.desc = d
         h = _P()
         _check(lib().moe_plan_create(ctypes.byref(d), ctypes.byref(h)))

@@ -390,22 +390,22 @@ expert_decode_kernel(ExpertArgs a) {
   const int gpb = kBlockK / G;  // scale groups per 256-column block
   const int sdt = a.sdt;
 
-  // shared memory carve-up (all offsets multiples of 16 bytes)
-  uint8_t* xs = sm;  // [T] fragment-ordered rows of the layer input
-  size_t off = (size_t)T * xrow;
-  float* csa = reinterpret_cast<float*>(sm + off);  // [ngH][9], column 8 = 0
-  off += ((size_t)ngH * 9 * 4 + 15) / 16 * 16;
-  uint8_t* hs = sm + off;  // [T] fragment-ordered rows of one expert's h
-  off += (size_t)T * hrow;
-  float* csb = reinterpret_cast<float*>(sm + off);  // [ngI][9], column 8 = 0
-  off += ((size_t)ngI * 9 * 4 + 15) / 16 * 16;
+  // shared memory carve-up (all offsets multiples of 16 bytes).  A CTA runs
+  // all of its A tasks before its first B unit, and the last A task ends with
+  // a barrier of every consumer warp, so the B units' operands (h and its
+  // group sums) reuse the A tasks' (x and its group sums): a deeper ring.
+  uint8_t* xs = sm;  // [T] fragment-ordered rows of the layer input (A tasks) ...
+  uint8_t* hs = sm;  // ... then [T] fragment-ordered rows of one expert's h (B units)
+  size_t off = (size_t)T * max(xrow, hrow);
+  float* csa = reinterpret_cast<float*>(sm + off);  // [ngH][9] (A) / [ngI][9] (B), column 8 = 0
+  float* csb = csa;
+  off += ((size_t)max(ngH, ngI) * 9 * 4 + 15) / 16 * 16;
   float* red = reinterpret_cast<float*>(sm + off);  // [2][kWarps][16][8] per-warp partials
   off += (size_t)2 * kWarps * 128 * 4;
 
   uint8_t* ring = sm + off;  // a.nslots units
 
-  for (int i = tid; i < ngH; i += blockDim.x) csa[i * 9 + 8] = 0.f;
-  for (int i = tid; i < ngI; i += blockDim.x) csb[i * 9 + 8] = 0.f;
+  for (int i = tid; i < max(ngH, ngI); i += blockDim.x) csa[i * 9 + 8] = 0.f;
 
   // ---- the layer input is not produced by the router: stage it first
   for (int t = 0; t < T; ++t)
@@ -428,7 +428,22 @@ expert_decode_kernel(ExpertArgs a) {
         }
       }
     }
+  // the residence tables are not written by the router (only by an earlier
+  // step end, complete before it started): pull them into L1 while waiting,
+  // so that the grouping's lookups after routing do not go to L2
+  if (warp == kWarps - 1)
+    for (int e0 = lane * 16; e0 < E; e0 += 32 * 16) {  // 16 pointers per 128-byte line
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a.blob_hbm + e0));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a.blob_host + e0));
+    }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // scale-group sums of x (written by the router) into shared memory, by the
+  // highest-numbered threads, so that the top-k warps start at once
+  for (int i = (int)blockDim.x - 1 - tid; i < T * ngH; i += blockDim.x) {
+    const int t = i / ngH, grp = i % ngH;
+    csa[grp * 9 + t] = __ldcg(a.xsum + i);
+  }
 
   // Softmax over a token's k logits (R.w[t*k + j], j < k, descending), one
   // lane per slot: w_j = exp(l_j - l_0) / sum_j exp(l_j - l_0), the sum in j order.
@@ -548,10 +563,6 @@ expert_decode_kernel(ExpertArgs a) {
       }
     }
     renormalise(t);
-  }
-  for (int i = tid; i < T * ngH; i += blockDim.x) {
-    const int t = i / ngH, grp = i % ngH;
-    csa[grp * 9 + t] = __ldcg(a.xsum + i);
   }
   __syncthreads();
 
@@ -1045,21 +1056,22 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
         (size_t)kBRows * KP * b / 8 + (size_t)(kBRows / kTileRows) * (KP / G) * kTileRows * ssz;
     cf.slot_bytes = (int)((std::max(a_unit, b_unit) + 127) / 128 * 128);
     const size_t ngH = H / G, ngI = KP / G;
-    const size_t fixed = (size_t)T * frag_row_bytes(H / kBlockK) + (ngH * 9 * 4 + 15) / 16 * 16 +
-                         (size_t)T * frag_row_bytes(KP / kBlockK) + (ngI * 9 * 4 + 15) / 16 * 16 +
-                         (size_t)2 * kWarps * 128 * 4;
+    const size_t fixed = (size_t)T * std::max(frag_row_bytes(H / kBlockK), frag_row_bytes(KP / kBlockK)) +
+                         (std::max(ngH, ngI) * 9 * 4 + 15) / 16 * 16 + (size_t)2 * kWarps * 128 * 4;
+    const void* kfn = b == 2   ? (const void*)expert_decode_kernel<2>
+                      : b == 3 ? (const void*)expert_decode_kernel<3>
+                               : (const void*)expert_decode_kernel<4>;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device);
     if (e != cudaSuccess) return e;
-    // ring depth: as many units as fit beside the static routing state (<= 8 KB)
-    const long avail = (long)optin - 8192 - (long)fixed;
+    cudaFuncAttributes fa{};
+    if ((e = cudaFuncGetAttributes(&fa, kfn)) != cudaSuccess) return e;
+    // ring depth: as many units as fit beside the static routing state
+    const long avail = (long)optin - (long)fa.sharedSizeBytes - (long)fixed;
     cf.nslots = (int)std::min<long>(kMaxRing, avail / cf.slot_bytes);
     if (cf.nslots < 2) return cudaErrorInvalidConfiguration;
     cf.smem = fixed + (size_t)cf.nslots * cf.slot_bytes;
     cf.rsmem = (size_t)kRouterTok * H * 4;
-    const void* kfn = b == 2   ? (const void*)expert_decode_kernel<2>
-                      : b == 3 ? (const void*)expert_decode_kernel<3>
-                               : (const void*)expert_decode_kernel<4>;
     if ((e = ensure_dynamic_smem(kfn, cf.smem)) != cudaSuccess) return e;
     if ((e = ensure_dynamic_smem((const void*)router_logits_kernel, cf.rsmem)) != cudaSuccess) return e;
     int per_sm = 0;

@@ -352,7 +352,7 @@ moe_status validate(const moe_plan_desc* d, std::string& why) {
     why = "LFU cache: num_layers * min(E, max_tokens * top_k) must be <= 50000 (misses queued per step)";
     return MOE_ERR_INVALID;
   }
-  if (d->host_overlap != 0 && d->host_overlap != 1) { why = "host_overlap must be 0 or 1"; return MOE_ERR_INVALID; }
+  if (d->reserved0 != 0) { why = "reserved0 must be zero"; return MOE_ERR_INVALID; }
   if (d->aging_period < 0) { why = "aging_period must be >= 0"; return MOE_ERR_INVALID; }
   return MOE_OK;
 }
