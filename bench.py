@@ -699,9 +699,10 @@ def run_cached(args):
     hbm_peak, peak_kind = _peaks()
     link_gbs, hbm_probe = probe_bandwidth(0, 1 << 30, 5)
     t0 = time.perf_counter()
-    plan, info = harness.build_plan(wl, gpu_gen=True)
+    L = args.cached_layers or wl.layers  # fewer layers: small cases for profiler captures
+    plan, info = harness.build_plan(wl, gpu_gen=True, layers=L)
     build_s = time.perf_counter() - t0
-    L, H, E, T = wl.layers, wl.hidden, wl.experts, 1
+    H, E, T = wl.hidden, wl.experts, 1
     S = args.cached_steps
     # per-step router biases (the drift random walk, accumulated in fp32 on the host)
     b0 = np.stack([info["routers"][l][1] for l in range(L)]).astype(np.float32)
@@ -772,7 +773,8 @@ def run_cached(args):
     st_all = plan.stats(-1)
     line = _common_line(
         args, "MoE decode tokens/s (cached 48-layer decode)", S / (total_ms * 1e-3), "tokens/s", total_ms / S,
-        {"workload": wl.desc.replace("2048 steps", f"{S} steps"), "tokens_per_step": 1,
+        {"workload": wl.desc.replace("2048 steps", f"{S} steps").replace("48 layers", f"{L} layers"),
+         "tokens_per_step": 1,
          "l2": "no flush: a step touches ~440 MB", "cuda_graph": True, "parallelism": "single GPU"},
         {"hit_rate": st_all["hits"] / max(st_all["accesses"], 1),
          "hit_rate_second_half": (st_all["hits"] - st_half["hits"]) / max(st_all["accesses"] - st_half["accesses"], 1),
@@ -1133,6 +1135,7 @@ def main():
     ap.add_argument("--prefetch-steps", type=int, default=512)
     ap.add_argument("--cpu-vs-uva-picks", type=int, default=6)
     ap.add_argument("--cached-steps", type=int, default=2048)
+    ap.add_argument("--cached-layers", type=int, default=0, help="cached: layers (default 48)")
     ap.add_argument("--tokens", type=int, default=0, help="prefill: batch size (default 8192)")
     args = ap.parse_args()
     if args.warmup < 3:

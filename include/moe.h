@@ -132,16 +132,24 @@ typedef struct moe_cache_stats_t {
 
 /* Create a plan: validates the shapes, checks the memory it will need
  * against free HBM (minus a headroom of max(1 GiB, 2%)) and returns
- * MOE_ERR_OOM instead of failing later; allocates the HBM expert arena
- * (STATIC) or slot arena (LFU), the pinned host arena (every expert not in
- * HBM; all experts under LFU) and all scratch.  *out is set on success. */
+ * MOE_ERR_OOM instead of failing later -- a plan that fits at load time and
+ * dies under load is the failure "125B sparse model on one 32 GB consumer
+ * card" describes in section "A compute buffer is what limits capacity";
+ * allocates the HBM expert arena (STATIC) or slot arena (LFU), the pinned host
+ * arena (every expert not in HBM; all experts under LFU) on the GPU's NUMA
+ * node where the system reports one ("763B MoE in two 96 GB cards", section
+ * "PCIe topology"), and all scratch.  *out is set on success.  Test hook:
+ * the environment variable MOE_FAULT containing "hbm_alloc" or
+ * "pinned_alloc" makes that allocation fail (MOE_ERR_OOM, all released). */
 moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out);
 
 /* Free everything the plan owns.  Waits for the plan's outstanding work. */
 moe_status moe_plan_destroy(moe_plan* plan);
 
-/* Router of `layer`: wr [E][H] bf16 (host or device), bias [E] fp32 (host or
- * device) or NULL for none.  Copied; synchronous. */
+/* Router of `layer` (the gate that picks k of the E routed experts per token,
+ * "763B MoE in two 96 GB cards", section "Where the VRAM gap comes from"):
+ * wr [E][H] bf16 (host or device), bias [E] fp32 (host or device) or NULL for
+ * none.  Copied; synchronous. */
 moe_status moe_set_router(moe_plan* plan, int layer, const uint16_t* wr_bf16, const float* bias);
 
 /* Replace the router bias of `layer` in stream order (bias [E] fp32, host or
@@ -156,8 +164,11 @@ moe_status moe_update_router_bias(moe_plan* plan, int layer, const float* bias, 
 moe_status moe_update_router_biases(moe_plan* plan, int first, int count, const float* bias,
                                     void* stream);
 
-/* Place experts first .. first+count-1 of `layer`: copy each expert from the
- * canonical format into its device layout at residence[i] (MOE_RES_HBM or
+/* Place experts first .. first+count-1 of `layer` -- the per-expert plan of
+ * "763B MoE in two 96 GB cards" (side-box of section "Same idea, native vLLM
+ * fails": each expert's residence and read path decided on its own): copy
+ * each expert from the canonical format into its device layout at
+ * residence[i] (MOE_RES_HBM or
  * MOE_RES_HOST; ignored under LFU, where every expert goes to host memory;
  * NULL = all HBM).  An expert may be placed again (its residence can change)
  * under STATIC; under LFU experts are placed once, before the first forward.
@@ -166,7 +177,10 @@ moe_status moe_update_router_biases(moe_plan* plan, int first, int count, const 
 moe_status moe_place_experts(moe_plan* plan, int layer, int first, int count,
                              const uint8_t* residence, const moe_expert_weights* w);
 
-/* Forward of `layer` on T tokens: x [T][H] bf16 device (16-byte aligned),
+/* Forward of `layer` on T tokens (route, group by expert, SwiGLU FFN of each
+ * chosen expert read from HBM or in place from pinned host memory over UVA,
+ * weighted combine: "763B MoE in two 96 GB cards", section "Where the VRAM gap
+ * comes from" and its UVA side-box): x [T][H] bf16 device (16-byte aligned),
  * y [T][H] bf16 device (must not alias x).  0 <= T <= max_tokens; T = 0 is a
  * no-op.  Every expert of the layer must have been placed.  Stream-ordered,
  * no host synchronisation inside: y is valid when `stream` reaches the end
@@ -185,8 +199,11 @@ moe_status moe_layer_forward_host(moe_plan* plan, int layer, const void* x_host,
 
 /* End of one decode step (one token through all layers).  Under LFU, runs the
  * admission/eviction pass over the step's misses and fills the admitted
- * experts' slots, in stream order; the next step sees the new residence.
- * Under STATIC it only advances the step counter. */
+ * experts' slots, in stream order; the next step sees the new residence --
+ * the cache that "adapts to the conversation" of "Running a 24k-expert MoE on
+ * a single 32 GB card", section 2 (rules of the pass: moe_plan_desc's
+ * cache_policy and aging_period).  Under STATIC it only advances the step
+ * counter. */
 moe_status moe_step_end(moe_plan* plan, void* stream);
 
 /* Counters of `layer` (or of all layers for layer = -1); reset = 1 zeroes
@@ -202,11 +219,17 @@ moe_status moe_step_end(moe_plan* plan, void* stream);
 moe_status moe_cache_stats(moe_plan* plan, int layer, moe_cache_stats_t* out, int reset);
 
 /* Residence of every expert of `layer` as seen by the next forward: out[e] =
- * slot index (>= 0, HBM) or -1 (host).  Under STATIC, slot = position in the
- * HBM arena.  Synchronous. */
+ * slot index (>= 0, HBM) or -1 (host) -- the per-expert residence of the
+ * per-expert plan ("763B MoE in two 96 GB cards", side-box of section "Same
+ * idea, native vLLM fails") or of the cache ("Running a 24k-expert MoE on a
+ * single 32 GB card", section 2).  Under STATIC, slot = position in the HBM
+ * arena.  Synchronous. */
 moe_status moe_residence_table(moe_plan* plan, int layer, int32_t* out_host);
 
-/* Quantise w [rows][cols] fp32 (device) into the canonical format: codes
+/* Quantise w [rows][cols] fp32 (device) into the canonical format (the
+ * low-bit expert weights of "763B MoE in two 96 GB cards", 3-bit, and of
+ * "Running a 24k-expert MoE on a single 32 GB card", 2-bit, read here as
+ * symmetric int-b group quantisation): codes
  * (device, rows*cols*bits/8 bytes) and scales (device, [rows][cols/group] in
  * scale_dtype), groups of `group` along cols.  Per group: s = amax / qmax
  * rounded to nearest-even in the scale dtype, q = clamp(rint(w / s), -qmax,
@@ -215,7 +238,8 @@ moe_status moe_quantize(const float* w, int rows, int cols, int bits, int group,
                         void* codes, void* scales, void* stream);
 
 /* Measure the GPU's zero-copy read bandwidth from pinned host memory (the
- * link host experts are read over) and its HBM read bandwidth, with a
+ * link host experts are read over: "763B MoE in two 96 GB cards", UVA side-box
+ * of section "Where the VRAM gap comes from") and its HBM read bandwidth, with a
  * streaming-read kernel over `bytes` bytes (>= 64 MiB recommended), best of
  * `iters` runs.  Synchronous; allocates and frees its own buffers. */
 moe_status moe_probe_bandwidth(int device, size_t bytes, int iters, double* host_read_gbs,

@@ -3,7 +3,11 @@
 // the link probe.  The forward passes live in decode.cu / prefill.cu and the
 // cache policy in cache.cu.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
+#include <sys/mman.h>
+#include <sys/syscall.h>
+#include <unistd.h>
 
 #include <algorithm>
 #include <map>
@@ -70,6 +74,72 @@ bool take_overflow(Plan* p) {
   if (!p->err_host || !p->err_host[1]) return false;
   p->err_host[1] = 0;
   return true;
+}
+
+// Host-side fault injection for the failure paths (tests): MOE_FAULT holds a
+// comma-separated list; "hbm_alloc" makes the plan's HBM arena allocation
+// fail, "pinned_alloc" its pinned host arena allocation.  Both then take the
+// same path as a real failure: everything allocated so far is released and
+// moe_plan_create returns MOE_ERR_OOM.  No device work is involved.
+bool fault_injected(const char* what) {
+  const char* f = getenv("MOE_FAULT");
+  return f && strstr(f, what) != nullptr;
+}
+
+// NUMA node of the plan's GPU (sysfs of its PCI function), or -1.
+int gpu_numa_node(int device) {
+  char bus[32] = {0};
+  if (cudaDeviceGetPCIBusId(bus, sizeof bus, device) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  for (char* c = bus; *c; ++c)
+    if (*c >= 'A' && *c <= 'F') *c = (char)(*c - 'A' + 'a');
+  char path[128];
+  snprintf(path, sizeof path, "/sys/bus/pci/devices/%s/numa_node", bus);
+  FILE* f = fopen(path, "r");
+  if (!f) return -1;
+  int node = -1;
+  if (fscanf(f, "%d", &node) != 1) node = -1;
+  fclose(f);
+  return node;
+}
+
+// Pinned, device-mapped host memory of `bytes`, placed on NUMA node `node`
+// when node >= 0 (anonymous mapping bound with mbind before the pages are
+// first touched, then page-locked and mapped by cudaHostRegister), else by
+// cudaHostAlloc.  *mapped reports which of the two (for the matching free).
+void* pinned_alloc(size_t bytes, int node, bool* mapped) {
+  *mapped = false;
+  if (node >= 0 && node < 64) {
+    void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (p != MAP_FAILED) {
+      unsigned long mask = 1ul << node;
+      const long rc = syscall(SYS_mbind, p, bytes, 2 /* MPOL_BIND */, &mask, 64ul, 0u);
+      if (rc == 0 && cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+        *mapped = true;
+        return p;
+      }
+      cudaGetLastError();
+      munmap(p, bytes);
+    }
+  }
+  void* h = nullptr;
+  if (cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return h;
+}
+
+void pinned_free(void* p, size_t bytes, bool mapped) {
+  if (!p) return;
+  if (mapped) {
+    cudaHostUnregister(p);
+    munmap(p, bytes);
+  } else {
+    cudaFreeHost(p);
+  }
 }
 
 bool is_device_ptr(const void* ptr) {
@@ -374,7 +444,7 @@ void release(Plan* p) {
                  p->miss_count, p->adm_list, p->adm_count, p->stats};
   for (void* v : dev)
     if (v) cudaFree(v);
-  if (p->host_arena) cudaFreeHost(p->host_arena);
+  pinned_free(p->host_arena, (size_t)(p->host_cap * p->lay.blob_bytes), p->host_mmap);
   if (p->err_host) cudaFreeHost((void*)p->err_host);
   if (p->aux) cudaStreamDestroy(p->aux);
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
@@ -454,16 +524,24 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
     }                                                        \
   } while (0)
 
+  if (slots > 0 && fault_injected("hbm_alloc")) {
+    release(p);
+    return fail(nullptr, MOE_ERR_OOM, "cudaMalloc p->hbm_arena (injected by MOE_FAULT=hbm_alloc)");
+  }
   if (slots > 0) ALLOC(p->hbm_arena, (size_t)(slots * p->lay.blob_bytes));
   if (host_n > 0) {
-    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&p->host_arena),
-                                  (size_t)(host_n * p->lay.blob_bytes),
-                                  cudaHostAllocMapped | cudaHostAllocPortable);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      p->host_arena = nullptr;
+    // on the GPU's own NUMA node ("763B MoE in two 96 GB cards", section "PCIe
+    // topology": host memory across the socket interconnect slows every link read)
+    p->numa_node = gpu_numa_node(d.device);
+    p->host_arena = fault_injected("pinned_alloc")
+                        ? nullptr
+                        : static_cast<uint8_t*>(pinned_alloc((size_t)(host_n * p->lay.blob_bytes), p->numa_node,
+                                                             &p->host_mmap));
+    if (!p->host_arena) {
       release(p);
-      return fail(nullptr, MOE_ERR_OOM, "pinned host arena allocation failed");
+      return fail(nullptr, MOE_ERR_OOM, fault_injected("pinned_alloc")
+                                            ? "pinned host arena allocation failed (injected by MOE_FAULT=pinned_alloc)"
+                                            : "pinned host arena allocation failed");
     }
     if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->host_arena_dev), p->host_arena, 0) !=
         cudaSuccess) {

@@ -365,3 +365,20 @@ def test_decode_activation_edge_cases(decode_layer, T, mode):
     ref = oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, wl.top_k, wl.bits, wl.group,
                                       wl.scale_dtype, x, wr, bias, np.arange(T))
     assert _rel_err(_bf16_bits_to_f64(y), ref) <= TOL
+
+
+@pytest.mark.parametrize("fault", ["pinned_alloc", "hbm_alloc"])
+def test_injected_allocation_failure_returns_oom(fault, monkeypatch):
+    """The host-side fault injection of the failure path: with MOE_FAULT set,
+    the pinned host arena (or the HBM arena) allocation fails as a real one
+    would, and moe_plan_create returns MOE_ERR_OOM with everything released;
+    without it the same plan is created."""
+    from moe_expert_layer_sorted_gb300 import MoeError, Plan
+    kw = dict(num_layers=1, num_experts=16, hidden=256, inter=128, top_k=2, weight_bits=4, group_size=32,
+              scale_dtype=0, max_tokens=8, hbm_experts=8)  # 8 experts in HBM, 8 in pinned host memory
+    monkeypatch.setenv("MOE_FAULT", fault)
+    with pytest.raises(MoeError) as ei:
+        Plan(**kw)
+    assert ei.value.status == 2 and "injected" in str(ei.value)
+    monkeypatch.delenv("MOE_FAULT")
+    Plan(**kw).close()
