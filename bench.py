@@ -1052,6 +1052,57 @@ def run_prefetch_bound(args):
     plan.close()
 
 
+def run_prefill_chunked(args):
+    """Chunked prefill with reserved slots (moe_prefill_forward): a long prompt
+    (T tokens, chunks of 8,192) through the decode layer with its 115
+    least-popular experts in pinned host memory, (a) staged once per prompt
+    into 115 prefill slots, (b) read in place from host memory by every chunk,
+    (c) on a plan with every expert in HBM."""
+    import torch
+    import synth
+    from moe_expert_layer_sorted_gb300 import harness
+    from synth import workloads as W
+    wl = W.WORKLOADS["decode"]
+    T = args.tokens or 131072  # the pages' 128K-token prompt
+    dev = torch.device("cuda", 0)
+    n_host = wl.host_count(0)
+    plans = {"staged": harness.build_plan(wl, max_tokens=8192, prefill_slots=n_host, gpu_gen=True)[0],
+             "in_place": harness.build_plan(wl, max_tokens=8192, prefill_slots=0, gpu_gen=True)[0],
+             "all_hbm": harness.build_plan(wl, max_tokens=8192, all_hbm=True, gpu_gen=True)[0]}
+    x = torch.empty(T, wl.hidden, dtype=torch.bfloat16, device=dev)
+    synth.normal_bf16_device(W.key(wl.seed, W.TAG_X, 900, 0), T * wl.hidden, 1.0, x.data_ptr(),
+                             torch.cuda.current_stream().cuda_stream)
+    y = torch.empty_like(x)
+    ms, stats = {}, {}
+    for name, plan in plans.items():
+        for _ in range(args.warmup):
+            plan.prefill_forward(0, x, y)
+        torch.cuda.synchronize()
+        plan.stats(0, reset=True)
+        ev = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            plan.prefill_forward(0, x, y)
+            b.record()
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        ms[name] = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        st = plan.stats(0, reset=True)
+        stats[name] = {k_: st[k_] / args.steps for k_ in ("host_bytes", "fill_bytes", "hits", "misses")}
+    for plan in plans.values():
+        plan.close()
+    line = _common_line(
+        args, "chunked prefill with reserved prefill slots (ms per prompt)", ms["staged"], "ms", ms["staged"],
+        {"workload": f"{T}-token prompt in chunks of 8,192 through the decode layer (H=4096, I=1024, E=384, "
+                     f"top-6, int3 G128), {n_host} least-popular experts in pinned host memory",
+         "parallelism": "single GPU"},
+        {"higher_is_better": False, "ms_staged_slots": ms["staged"], "ms_in_place": ms["in_place"],
+         "ms_all_hbm": ms["all_hbm"], "per_prompt": stats,
+         "tokens_per_s_staged": T / (ms["staged"] * 1e-3), "gpu_launches": None})
+    print(json.dumps(line), flush=True)
+
+
 def run_prefill_staging(args):
     """Prefill with host-resident experts: the tcgen05 GEMMs reading the host
     experts' codes in place over the link (bulk-copy warp, 16-byte cp.async)
@@ -1131,7 +1182,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="decode: leave out the prefill key")
     ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
                                                               "cpu-vs-uva", "prefetch-bound",
-                                                              "prefill-staging"])
+                                                              "prefill-staging", "prefill-chunked"])
     ap.add_argument("--prefetch-steps", type=int, default=512)
     ap.add_argument("--cpu-vs-uva-picks", type=int, default=6)
     ap.add_argument("--cached-steps", type=int, default=2048)
@@ -1154,6 +1205,8 @@ def main():
         run_prefetch_bound(args)
     elif args.workload == "prefill-staging":
         run_prefill_staging(args)
+    elif args.workload == "prefill-chunked":
+        run_prefill_chunked(args)
     else:
         run_ours(args)
 

@@ -87,7 +87,9 @@ typedef struct moe_plan_desc {
   int32_t reserved0;    /* must be zero (host- and HBM-resident experts are always processed
                            by one grid, with a share of its CTAs given to the host experts) */
   int32_t aging_period; /* LFU: halve all access counts every aging_period steps (0 = never) */
-  int64_t reserved[4];  /* must be zero */
+  int64_t prefill_slots; /* HBM slots reserved for staging a long prompt's experts that are
+                            not in HBM (moe_prefill_forward); 0 = none */
+  int64_t reserved[3];   /* must be zero */
 } moe_plan_desc;
 
 /* One expert in the canonical interchange format.  Matrices: gate Wg [I][H],
@@ -189,6 +191,24 @@ moe_status moe_place_experts(moe_plan* plan, int layer, int first, int count,
  * dbg may be NULL. */
 moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x_bf16, int T, void* y_bf16,
                              void* stream, const moe_routing_out* dbg);
+
+/* Chunked prefill of a long prompt through `layer`: the prefill-aware cache of
+ * "Running a 24k-expert MoE on a single 32 GB card", section 2 -- HBM slots
+ * kept for the prompt's experts, and long inputs read in chunks of 8,192
+ * tokens.  x [T][H] and y [T][H] bf16 device (16-byte aligned, not aliased),
+ * any T >= 0; needs max_tokens > 8 (the chunks, min(8192, max_tokens) tokens
+ * each, take the prefill path of moe_layer_forward).  When there is more than
+ * one chunk, the layer's experts that are not in HBM (host-resident; under LFU
+ * those the cache does not hold) are first copied into the plan's
+ * prefill_slots, in ascending expert order as far as the slots go, and every
+ * chunk reads the staged copies (the rest in place from pinned host memory):
+ * each such expert crosses the host link once per prompt, not once per chunk.  These forwards leave the
+ * LFU state untouched (no access counts, no misses queued), so a prompt that
+ * routes to nearly every expert neither evicts nor retrains the decode cache;
+ * moe_cache_stats counts their reads (staged experts as HBM hits) and the
+ * staging copies (fill_bytes).  Stream-ordered like moe_layer_forward. */
+moe_status moe_prefill_forward(moe_plan* plan, int layer, const void* x_bf16, int64_t T, void* y_bf16,
+                               void* stream);
 
 /* Same layer forward with HOST buffers: copies x (host [T][H] bf16) into the
  * plan's device staging buffer, runs the forward and copies y back into

@@ -26,7 +26,8 @@ POLICY_STATIC, POLICY_LFU = 0, 1
 # every symbol include/moe.h declares
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_set_router", "moe_update_router_bias",
            "moe_update_router_biases", "moe_debug_fail_next_forward",
-           "moe_place_experts", "moe_layer_forward", "moe_layer_forward_host", "moe_step_end",
+           "moe_place_experts", "moe_layer_forward", "moe_prefill_forward", "moe_layer_forward_host",
+           "moe_step_end",
            "moe_cache_stats", "moe_residence_table", "moe_quantize", "moe_probe_bandwidth",
            "moe_route_noalloc", "moe_status_string", "moe_last_error"]
 
@@ -48,7 +49,7 @@ class PlanDesc(ctypes.Structure):
                 ("cache_policy", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("hbm_experts", ctypes.c_int64), ("cache_slots", ctypes.c_int64),
                 ("reserved0", ctypes.c_int32), ("aging_period", ctypes.c_int32),
-                ("reserved", ctypes.c_int64 * 4)]
+                ("prefill_slots", ctypes.c_int64), ("reserved", ctypes.c_int64 * 3)]
 
 
 class ExpertWeights(ctypes.Structure):
@@ -87,6 +88,7 @@ def lib():
         L.moe_place_experts.argtypes = [_P, i32, i32, i32, _P, ctypes.POINTER(ExpertWeights)]
         L.moe_layer_forward.argtypes = [_P, i32, _P, i32, _P, _P, ctypes.POINTER(RoutingOut)]
         L.moe_layer_forward_host.argtypes = [_P, i32, _P, i32, _P, _P]
+        L.moe_prefill_forward.argtypes = [_P, i32, _P, ctypes.c_int64, _P, _P]
         L.moe_step_end.argtypes = [_P, _P]
         L.moe_cache_stats.argtypes = [_P, i32, ctypes.POINTER(CacheStats), i32]
         L.moe_residence_table.argtypes = [_P, i32, _P]
@@ -140,7 +142,7 @@ class Plan:
 
     def __init__(self, *, num_layers, num_experts, hidden, inter, top_k, weight_bits, group_size,
                  scale_dtype, max_tokens, cache_policy=POLICY_STATIC, hbm_experts=0,
-                 cache_slots=0, aging_period=0, device=0):
+                 cache_slots=0, aging_period=0, prefill_slots=0, device=0):
         d = PlanDesc()
         d.struct_size = ctypes.sizeof(PlanDesc)
         d.num_layers, d.num_experts, d.hidden, d.inter = num_layers, num_experts, hidden, inter
@@ -148,6 +150,7 @@ class Plan:
         d.max_tokens, d.cache_policy, d.device = max_tokens, cache_policy, device
         d.hbm_experts, d.cache_slots = hbm_experts, cache_slots
         d.aging_period = aging_period
+        d.prefill_slots = prefill_slots
         self.desc = d
         h = _P()
         _check(lib().moe_plan_create(ctypes.byref(d), ctypes.byref(h)))
@@ -205,6 +208,11 @@ class Plan:
                 setattr(ro, k, _addr(v))
             ro = ctypes.byref(ro)
         _check(lib().moe_layer_forward(self._h, layer, _addr(x), T, _addr(y), _stream(stream), ro),
+               self._h)
+
+    def prefill_forward(self, layer, x, y, stream=None):
+        """Chunked prefill of a long prompt with the plan's prefill slots (see moe.h)."""
+        _check(lib().moe_prefill_forward(self._h, layer, _addr(x), int(x.shape[0]), _addr(y), _stream(stream)),
                self._h)
 
     def forward_host(self, layer, x_host, y_host, stream=None):

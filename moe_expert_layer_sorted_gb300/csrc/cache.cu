@@ -167,7 +167,71 @@ __global__ void lfu_fill_kernel(const unsigned* __restrict__ adm, const unsigned
   }
 }
 
+// The chunked prefill's residence of one layer ("Running a 24k-expert MoE on a
+// single 32 GB card", section 2: slots kept for a prompt's experts): an expert
+// with an HBM copy keeps it; the others, in ascending expert order, take the
+// prefill slots while they last (the rest stay host-only).  stage[0] = number
+// staged; stage[2 + 2i], stage[3 + 2i] = (global id, slot) of the i-th, for
+// the fill kernel.  The staged bytes count as fill bytes of the layer.
+__global__ void __launch_bounds__(1024) pf_stage_kernel(const uint8_t* const* __restrict__ blob_hbm, int E,
+                                                        int64_t ge0, int64_t nslots, uint8_t* arena,
+                                                        int64_t blob_bytes, const uint8_t** pf_blob,
+                                                        unsigned* stage, unsigned long long* stats,
+                                                        int64_t expert_bytes) {
+  __shared__ unsigned wsum[32];
+  __shared__ unsigned carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  if (tid == 0) carry_s = 0u;
+  __syncthreads();
+  for (int base = 0; base < E; base += blockDim.x) {
+    const int e = base + tid;
+    const uint8_t* hb = e < E ? blob_hbm[e] : nullptr;
+    const bool flag = e < E && hb == nullptr;
+    const unsigned bal = __ballot_sync(0xffffffffu, flag);
+    if (lane == 0) wsum[warp] = __popc(bal);
+    __syncthreads();
+    unsigned before = carry_s;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    const unsigned rank = before + __popc(bal & ((1u << lane) - 1u));
+    if (e < E) {
+      if (!flag) {
+        pf_blob[e] = hb;
+      } else if ((int64_t)rank < nslots) {
+        pf_blob[e] = arena + (int64_t)rank * blob_bytes;
+        stage[2 + 2 * rank] = (unsigned)(ge0 + e);
+        stage[3 + 2 * rank] = rank;
+      } else {
+        pf_blob[e] = nullptr;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned tot = 0;
+      for (int w = 0; w < nw; ++w) tot += wsum[w];
+      carry_s += tot;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const unsigned n = (unsigned)min((int64_t)carry_s, nslots);
+    stage[0] = n;
+    stats[kStatFillBytes] += (unsigned long long)n * (unsigned long long)expert_bytes;
+  }
+}
+
 }  // namespace
+
+cudaError_t moe::prefill_stage(Plan& p, int layer, cudaStream_t s) {
+  const int E = p.d.num_experts;
+  const int64_t ge0 = (int64_t)layer * E;
+  pf_stage_kernel<<<1, 1024, 0, s>>>(p.blob_hbm + ge0, E, ge0, p.d.prefill_slots, p.pf_arena, p.lay.blob_bytes,
+                                     p.pf_blob, p.pf_stage, p.stats + (int64_t)layer * kNumStats,
+                                     p.lay.algo_bytes);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.d.prefill_slots == 0) return e;
+  lfu_fill_kernel<<<2 * p.sms, 512, 0, s>>>(p.pf_stage, p.pf_stage + 2, p.blob_host, p.pf_arena, p.lay.blob_bytes);
+  return cudaGetLastError();
+}
 
 cudaError_t moe::lfu_step_end(Plan& p, cudaStream_t s) {
   const moe_plan_desc& d = p.d;

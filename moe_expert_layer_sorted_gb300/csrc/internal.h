@@ -77,6 +77,9 @@ struct Plan {
 
   // arenas
   uint8_t* hbm_arena = nullptr;  // STATIC: experts; LFU: slots
+  uint8_t* pf_arena = nullptr;   // prefill_slots staging slots of a chunked prefill
+  const uint8_t** pf_blob = nullptr;  // [E] the chunked prefill's residence of one layer
+  unsigned* pf_stage = nullptr;       // [2] counts, then [E] (expert, slot) pairs staged
   int64_t hbm_cap = 0, hbm_used = 0;
   uint8_t* host_arena = nullptr;      // pinned, mapped
   uint8_t* host_arena_dev = nullptr;  // its device alias
@@ -171,7 +174,13 @@ cudaError_t launch_quantize(const float* w, int rows, int cols, int bits, int gr
 cudaError_t decode_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
                            cudaStream_t s, const moe_routing_out* dbg);
 cudaError_t lfu_step_end(Plan& p, cudaStream_t s);
+// lfu = false: the forward leaves the LFU state (counts, miss queue) as it is;
+// blob_hbm: the layer's HBM residence table to read (nullptr: the plan's own).
 cudaError_t prefill_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y, cudaStream_t s,
-                            const moe_routing_out* dbg);
+                            const moe_routing_out* dbg, bool lfu = true,
+                            const uint8_t* const* blob_hbm = nullptr);
+// Stages the layer's experts that are not in HBM into the prefill slots and
+// builds p.pf_blob (stream-ordered).
+cudaError_t prefill_stage(Plan& p, int layer, cudaStream_t s);
 
 }  // namespace moe

@@ -388,8 +388,12 @@ moe_status validate(const moe_plan_desc* d, std::string& why) {
     why = "struct_size != sizeof(moe_plan_desc)";
     return MOE_ERR_INVALID;
   }
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (d->reserved[i]) { why = "reserved fields must be zero"; return MOE_ERR_INVALID; }
+  if (d->prefill_slots < 0 || d->prefill_slots > d->num_experts) {
+    why = "prefill_slots must be in [0, num_experts]";
+    return MOE_ERR_INVALID;
+  }
   if (d->num_layers < 1 || d->num_experts < 1 || d->num_experts > 4096) {
     why = "need num_layers >= 1 and 1 <= num_experts <= 4096";
     return MOE_ERR_INVALID;
@@ -437,7 +441,7 @@ void release(Plan* p) {
   cudaDeviceSynchronize();
   for (auto* w : p->wr) cudaFree(w);
   cudaFree(p->bias_all);
-  void* dev[] = {p->hbm_arena, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
+  void* dev[] = {p->hbm_arena, p->pf_arena, p->pf_blob, p->pf_stage, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
                  p->wl_blob, p->ctl, p->hbuf, p->obuf, p->pf_h, p->pf_o, p->pf_bucket, p->xsum, p->x_stage,
                  p->y_stage, p->slot_of, p->slot_owner, p->lfu_count, p->lfu_last, p->miss_list,
@@ -498,7 +502,8 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   const int64_t lfu = d.cache_policy == MOE_POLICY_LFU
                           ? LE * 12 + slots * 8 + (int64_t)d.num_layers * maxD * 8
                           : 0;
-  const int64_t need = slots * p->lay.blob_bytes + (int64_t)d.num_layers * E * (H * 2 + 4) +
+  const int64_t need = (slots + d.prefill_slots) * p->lay.blob_bytes + E * 8 * 3 +
+                       (int64_t)d.num_layers * E * (H * 2 + 4) +
                        LE * 16 + scratch + lfu + (int64_t)d.num_layers * kNumStats * 8;
   size_t free_b = 0, total_b = 0;
   if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
@@ -529,6 +534,9 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
     return fail(nullptr, MOE_ERR_OOM, "cudaMalloc p->hbm_arena (injected by MOE_FAULT=hbm_alloc)");
   }
   if (slots > 0) ALLOC(p->hbm_arena, (size_t)(slots * p->lay.blob_bytes));
+  if (d.prefill_slots > 0) ALLOC(p->pf_arena, (size_t)(d.prefill_slots * p->lay.blob_bytes));
+  ALLOC(p->pf_blob, E);
+  ALLOC(p->pf_stage, 2 * E + 2);
   if (host_n > 0) {
     // on the GPU's own NUMA node ("763B MoE in two 96 GB cards", section "PCIe
     // topology": host memory across the socket interconnect slows every link read)
@@ -853,6 +861,51 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
   if (T <= kDecodeMaxTokens) e = decode_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
   else e = prefill_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
   if (e != cudaSuccess) return cuda_fail(p, e, "forward launch");
+  CK(p, cudaEventRecord(p->ev_done, s));
+  p->last_stream = s;
+  p->have_last = true;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void* x, int64_t T, void* y,
+                                          void* stream) {
+  Plan* p = reinterpret_cast<Plan*>(plan);
+  if (!p) return fail(nullptr, MOE_ERR_INVALID, "plan is NULL");
+  Busy b(p);
+  if (!b.ok) return fail(p, MOE_ERR_STATE, "plan is in use by another thread");
+  const moe_plan_desc& d = p->d;
+  if (layer < 0 || layer >= d.num_layers) return fail(p, MOE_ERR_INVALID, "bad layer");
+  if (T < 0) return fail(p, MOE_ERR_INVALID, "T < 0");
+  if (T == 0) return MOE_OK;
+  if (d.max_tokens <= kDecodeMaxTokens)
+    return fail(p, MOE_ERR_UNSUPPORTED, "chunked prefill needs max_tokens > 8 (prefill-path chunks)");
+  if (!x || !y || x == y) return fail(p, MOE_ERR_INVALID, "x and y must be distinct non-NULL device buffers");
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15))
+    return fail(p, MOE_ERR_INVALID, "x and y must be 16-byte aligned");
+  const int64_t base = (int64_t)layer * d.num_experts;
+  for (int e = 0; e < d.num_experts; ++e)
+    if (!p->placed[base + e]) return fail(p, MOE_ERR_STATE, "every expert of the layer must be placed first");
+  DeviceScope ds(p->d.device);
+  if (*p->err_host) return fail(p, MOE_ERR_STATE, "a latched device error is pending: call moe_layer_forward");
+  if (take_overflow(p)) return fail(p, MOE_ERR_STATE, kOverflowMsg);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (p->have_last && p->last_stream != s) CK(p, cudaStreamWaitEvent(s, p->ev_done, 0));
+  const int64_t chunk = std::min<int64_t>(8192, d.max_tokens), H = d.hidden;
+  // Staging pays back only over several chunks (it moves each host expert
+  // over the link once instead of once per chunk): with one chunk every
+  // expert is read in place.  The copies precede the first chunk; overlapping
+  // them with a first chunk that reads the same experts in place was measured
+  // slower, both sharing the link.
+  const bool stage = T > chunk && d.prefill_slots > 0;
+  cudaError_t e = cudaSuccess;
+  if (stage && (e = prefill_stage(*p, layer, s)) != cudaSuccess) return cuda_fail(p, e, "prefill staging");
+  for (int64_t off = 0; off < T; off += chunk) {
+    const int tc = (int)std::min<int64_t>(chunk, T - off);
+    e = prefill_forward(*p, layer, static_cast<const uint16_t*>(x) + off * H, tc,
+                        static_cast<uint16_t*>(y) + off * H, s, nullptr, /*lfu=*/false,
+                        stage ? p->pf_blob : nullptr);
+    if (e != cudaSuccess) return cuda_fail(p, e, "prefill chunk");
+  }
   CK(p, cudaEventRecord(p->ev_done, s));
   p->last_stream = s;
   p->have_last = true;

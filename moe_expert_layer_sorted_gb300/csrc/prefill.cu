@@ -1008,7 +1008,8 @@ size_t gemm_smem(const GemmArgs& a, int E) {
 }  // namespace
 
 cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
-                                 cudaStream_t s, const moe_routing_out* dbg) {
+                                 cudaStream_t s, const moe_routing_out* dbg, bool lfu,
+                                 const uint8_t* const* blob_hbm) {
   const moe_plan_desc& d = p.d;
   const int E = d.num_experts, H = d.hidden, I = d.inter, k = d.top_k;
   const int n = T * k;
@@ -1042,7 +1043,8 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   g.k = k;
   g.sdt = d.scale_dtype;
   g.G = G;
-  g.blob_hbm = p.blob_hbm + ge0;
+  const uint8_t* const* bhbm = blob_hbm ? blob_hbm : p.blob_hbm + ge0;
+  g.blob_hbm = bhbm;
   g.blob_host = p.blob_host + ge0;
   g.offsets = p.offsets;
   g.perm = p.perm;
@@ -1087,9 +1089,9 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     if ((e = launch_gemm<false>(d.weight_bits, map, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
   pf_combine_kernel<<<4 * p.sms, 256, 0, s>>>(p.pf_o, p.inv, T, H, k, y);
-  pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, p.blob_hbm + ge0, p.stats + (int64_t)layer * kNumStats,
+  pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, bhbm, p.stats + (int64_t)layer * kNumStats,
                                     p.lay.algo_bytes, (int64_t)E * H * 2, n,
-                                    d.cache_policy == MOE_POLICY_LFU, ge0, p.lfu_count, p.lfu_last,
+                                    lfu && d.cache_policy == MOE_POLICY_LFU, ge0, p.lfu_count, p.lfu_last,
                                     &p.ctl->step, p.miss_list, p.miss_count, d.num_layers * p.max_distinct,
                                     p.err_dev + 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

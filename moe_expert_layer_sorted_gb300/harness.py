@@ -53,7 +53,7 @@ class ExpertQuantiser:
 
 def build_plan(wl: W.Workload, *, max_tokens: int | None = None, layers: int | None = None,
                device: int = 0, all_hbm: bool = False, progress=None,
-               gpu_gen: bool = False, aging_period: int = 0):
+               gpu_gen: bool = False, aging_period: int = 0, prefill_slots: int = 0):
     """Create a plan for `wl` (first `layers` layers), set its routers and place
     every expert (host-resident ones per the workload; with all_hbm, a static
     plan with every expert in HBM).  Returns (plan, info)."""
@@ -74,7 +74,7 @@ def build_plan(wl: W.Workload, *, max_tokens: int | None = None, layers: int | N
                 cache_policy=POLICY_LFU if lfu else POLICY_STATIC,
                 hbm_experts=0 if lfu else L * wl.experts - n_host,
                 cache_slots=int(np.floor(wl.cache_frac * L * wl.experts)) if lfu else 0,
-                aging_period=aging_period, device=device)
+                aging_period=aging_period, prefill_slots=prefill_slots, device=device)
     q = ExpertQuantiser(wl, device=f"cuda:{device}", gpu_gen=gpu_gen)
     for l in range(L):
         wr, bias, _ = routers[l]
