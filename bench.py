@@ -1052,6 +1052,34 @@ def run_prefetch_bound(args):
     plan.close()
 
 
+def run_forwards(args):
+    """A few decode-layer forwards for profiler captures: T tokens (--tokens,
+    default 1), an input whose experts are all HBM-resident (so the captured
+    launches show the HBM path alone), one configuration forward, then
+    --steps forwards of that input.  Prints a short JSON line."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    from synth import workloads as W
+    wl = W.WORKLOADS["decode"]
+    T = args.tokens or 1
+    dev = torch.device("cuda", 0)
+    plan, info = harness.build_plan(wl)
+    y = torch.empty(T, wl.hidden, dtype=torch.bfloat16, device=dev)
+    for s_ in range(256):  # the first input routed to HBM experts only
+        x = torch.from_numpy(W.tokens(wl, 5000 + s_, 0, T).view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        plan.stats(0, reset=True)
+        plan.forward(0, x, y)
+        torch.cuda.synchronize()
+        if plan.stats(0, reset=True)["misses"] == 0:
+            break
+    for _ in range(args.steps):
+        plan.forward(0, x, y)
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": f"decode layer forwards at T={T} (input {s_}, HBM experts only)",
+                      "forwards": args.steps + s_ + 1}), flush=True)
+    plan.close()
+
+
 def run_prefill_chunked(args):
     """Chunked prefill with reserved slots (moe_prefill_forward): a long prompt
     (T tokens, chunks of 8,192) through the decode layer with its 115
@@ -1182,7 +1210,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="decode: leave out the prefill key")
     ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
                                                               "cpu-vs-uva", "prefetch-bound",
-                                                              "prefill-staging", "prefill-chunked"])
+                                                              "prefill-staging", "prefill-chunked",
+                                                              "forwards"])
     ap.add_argument("--prefetch-steps", type=int, default=512)
     ap.add_argument("--cpu-vs-uva-picks", type=int, default=6)
     ap.add_argument("--cached-steps", type=int, default=2048)
@@ -1207,6 +1236,8 @@ def main():
         run_prefill_staging(args)
     elif args.workload == "prefill-chunked":
         run_prefill_chunked(args)
+    elif args.workload == "forwards":
+        run_forwards(args)
     else:
         run_ours(args)
 
