@@ -878,9 +878,12 @@ def prefill_measure(args, steps: int, warmup: int, cpu: bool = True) -> dict:
                      "kernel": "whole prefill forward (router, grouping, tcgen05 gate/up and down GEMMs, combine)",
                      "peak_note": f"dense bf16, {tkind} burst figure; FLOPs = 6*T*k*H*I (expert FFNs) + 2*T*E*H (router)"},
         "cache": {k_: st[k_] for k_ in ("accesses", "hits", "hbm_bytes")},
+        "router_exact_per_token": st["router_exact"] / (steps * T),
         "e2e": {"value": T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2},
-        "setup_s": build_s, "gpu_launches": 10 * steps, "clocks": ck}
+        "setup_s": build_s, "gpu_launches": 9 * steps,
+        "gpu_launches_note": "the library's own kernels; the router's approximate-logit GEMM is a cuBLAS launch "
+                             "on top", "clocks": ck}
     if cpu:
         cores = os.cpu_count() or 1
         v, dt, sample = cpu_baseline(wl, 2 * cores, cores, seed_base=600)

@@ -130,6 +130,9 @@ typedef struct moe_cache_stats_t {
   uint64_t fill_bytes; /* LFU: bytes written into HBM slots by admissions */
   uint64_t pairs;      /* (token, expert) pairs computed */
   uint64_t forwards;   /* layer forwards */
+  uint64_t router_exact; /* prefill path: router logits computed in the library's fixed
+                          * order -- T*E when the logits are requested, otherwise the
+                          * candidates the bounded tensor-core pass leaves per token */
 } moe_cache_stats_t;
 
 /* Create a plan: validates the shapes, checks the memory it will need

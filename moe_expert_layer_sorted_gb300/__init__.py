@@ -64,7 +64,7 @@ class RoutingOut(ctypes.Structure):
 class CacheStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("accesses", "hits", "misses", "admissions", "evictions", "hbm_bytes",
-                 "host_bytes", "fill_bytes", "pairs", "forwards")]
+                 "host_bytes", "fill_bytes", "pairs", "forwards", "router_exact")]
 
 
 _lib = None

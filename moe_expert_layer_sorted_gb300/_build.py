@@ -53,7 +53,8 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 if r.returncode:
                     raise RuntimeError(f"nvcc failed for {j[-3]}")
     if jobs or force or not os.path.exists(LIB):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
+        cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
+        cmd = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-lcublas", "-Xlinker", f"-rpath,{cuda_lib}"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             print(" ".join(cmd))

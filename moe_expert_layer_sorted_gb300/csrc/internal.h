@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -56,7 +57,7 @@ inline int scale_size(int dt) { return dt == MOE_SCALE_F32 ? 4 : 2; }
 // Device counters per layer (uint64): order must match kStat*.
 enum {
   kStatAccesses = 0, kStatHits, kStatMisses, kStatAdmissions, kStatEvictions, kStatHbmBytes,
-  kStatHostBytes, kStatFillBytes, kStatPairs, kStatForwards, kNumStats
+  kStatHostBytes, kStatFillBytes, kStatPairs, kStatForwards, kStatRouterExact, kNumStats
 };
 
 // Error bits latched by kernels into the plan's error word.
@@ -99,6 +100,11 @@ struct Plan {
   std::vector<uint16_t*> wr;  // device [E][H] bf16 per layer
   std::vector<float*> bias;   // device [E] per layer (zeros when none), rows of bias_all
   float* bias_all = nullptr;  // device [L][E]
+  float* wnorm_all = nullptr;  // device [L][E] upper bounds of the router rows' 2-norms
+  // prefill routing: cuBLAS handle with a workspace of its own (no allocation in a forward)
+  cublasHandle_t blas = nullptr;
+  void* blas_ws = nullptr;
+  static constexpr size_t kBlasWorkspace = size_t(32) << 20;
 
   // forward scratch (device)
   float* logits = nullptr;            // [maxT][E]
@@ -166,6 +172,7 @@ struct Plan {
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
 // Launchers implemented in the .cu files (return cudaError_t of the launch).
+cudaError_t router_norms(const uint16_t* wr, int E, int H, float* out, cudaStream_t s);
 cudaError_t launch_repack(const uint8_t* src_codes, const void* src_scales, uint8_t* dst_blob,
                           const MatLayout& m, int bits, int group, int scale_dtype,
                           cudaStream_t s);

@@ -441,6 +441,9 @@ void release(Plan* p) {
   cudaDeviceSynchronize();
   for (auto* w : p->wr) cudaFree(w);
   cudaFree(p->bias_all);
+  cudaFree(p->wnorm_all);
+  if (p->blas) cublasDestroy(p->blas);
+  cudaFree(p->blas_ws);
   void* dev[] = {p->hbm_arena, p->pf_arena, p->pf_blob, p->pf_stage, p->blob_hbm, p->blob_host, p->logits, p->topk_idx, p->topk_w,
                  p->counts, p->offsets, p->perm, p->inv, p->wl_expert, p->wl_off, p->wl_cnt,
                  p->wl_blob, p->ctl, p->hbuf, p->obuf, p->pf_h, p->pf_o, p->pf_bucket, p->xsum, p->x_stage,
@@ -504,7 +507,8 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
                           : 0;
   const int64_t need = (slots + d.prefill_slots) * p->lay.blob_bytes + E * 8 * 3 +
                        (int64_t)d.num_layers * E * (H * 2 + 4) +
-                       LE * 16 + scratch + lfu + (int64_t)d.num_layers * kNumStats * 8;
+                       LE * 16 + scratch + lfu + (int64_t)d.num_layers * kNumStats * 8 + LE * 4 +
+                       (maxT > kDecodeMaxTokens ? (int64_t)Plan::kBlasWorkspace : 0);
   size_t free_b = 0, total_b = 0;
   if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
     release(p);
@@ -593,6 +597,7 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   ALLOC(p->x_stage, maxT * H);
   ALLOC(p->y_stage, maxT * H);
   ALLOC(p->stats, (int64_t)d.num_layers * kNumStats);
+  ALLOC(p->wnorm_all, LE);
   if (d.cache_policy == MOE_POLICY_LFU) {
     ALLOC(p->slot_of, LE);
     ALLOC(p->slot_owner, std::max<int64_t>(slots, 1));
@@ -602,6 +607,22 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
     ALLOC(p->miss_count, 1);
     ALLOC(p->adm_list, 2 * (int64_t)d.num_layers * maxD + 2);
     ALLOC(p->adm_count, 4);
+  }
+  if (maxT > kDecodeMaxTokens) {  // prefill routing's tensor-core logits
+    uint8_t* ws = nullptr;
+    ALLOC(ws, Plan::kBlasWorkspace);
+    p->blas_ws = ws;
+    if (cublasCreate(&p->blas) != CUBLAS_STATUS_SUCCESS) {
+      p->blas = nullptr;
+      cudaGetLastError();
+      release(p);
+      return fail(nullptr, MOE_ERR_CUDA, "cublasCreate failed");
+    }
+    if (cublasSetWorkspace(p->blas, p->blas_ws, Plan::kBlasWorkspace) != CUBLAS_STATUS_SUCCESS ||
+        cublasSetPointerMode(p->blas, CUBLAS_POINTER_MODE_HOST) != CUBLAS_STATUS_SUCCESS) {
+      release(p);
+      return fail(nullptr, MOE_ERR_CUDA, "cuBLAS workspace set-up failed");
+    }
   }
 #undef ALLOC
   p->wr.assign(d.num_layers, nullptr);
@@ -627,6 +648,7 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   cudaMemset(p->hbuf, 0, (size_t)maxD * decT * (KPI / 2) * 8);  // epoch 0: never current
   cudaMemset(p->obuf, 0, (size_t)decT * k * H * 8);
   cudaMemset(p->stats, 0, (size_t)d.num_layers * kNumStats * 8);
+  cudaMemset(p->wnorm_all, 0, LE * 4);  // the routers start as zeros
   if (d.cache_policy == MOE_POLICY_LFU) {
     cudaMemset(p->slot_of, 0xff, LE * 4);
     cudaMemset(p->slot_owner, 0xff, std::max<int64_t>(slots, 1) * 4);
@@ -676,6 +698,8 @@ extern "C" moe_status moe_set_router(moe_plan* plan, int layer, const uint16_t* 
   CK(p, cudaMemcpy(p->wr[layer], wr, E * H * 2, cudaMemcpyDefault));
   if (bias) CK(p, cudaMemcpy(p->bias[layer], bias, E * 4, cudaMemcpyDefault));
   else CK(p, cudaMemset(p->bias[layer], 0, E * 4));
+  CK(p, router_norms(p->wr[layer], (int)E, (int)H, p->wnorm_all + layer * E, nullptr));
+  CK(p, cudaDeviceSynchronize());
   return MOE_OK;
 }
 
@@ -973,6 +997,7 @@ extern "C" moe_status moe_cache_stats(moe_plan* plan, int layer, moe_cache_stats
   out->fill_bytes = acc[kStatFillBytes];
   out->pairs = acc[kStatPairs];
   out->forwards = acc[kStatForwards];
+  out->router_exact = acc[kStatRouterExact];
   if (reset) {
     if (layer < 0) CK(p, cudaMemset(p->stats, 0, h.size() * 8));
     else CK(p, cudaMemset(p->stats + (size_t)layer * kNumStats, 0, kNumStats * 8));

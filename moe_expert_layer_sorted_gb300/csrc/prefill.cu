@@ -163,17 +163,17 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const uint16_t* __restri
     }
 }
 
-// One warp per token: k rounds of (lane's best untaken logit, warp max by an
-// order-preserving key, warp min of the index among the lanes holding it);
-// lanes scan experts lane, lane+32, ... so ties resolve to the lower index.
-__global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                               int32_t* __restrict__ idx, float* __restrict__ wout) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* l = logits + (int64_t)t * E;
-  int chosen[kMaxTopK];
-  float cv[kMaxTopK];
+// Order-preserving key of a logit (-0 and +0 equal): a > b  <=>  key(a) > key(b).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t ub = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (ub & 0x80000000u) ? ~ub : (ub | 0x80000000u);
+}
+
+// The k largest entries of a token's logit row l[0..E) (one warp): k rounds of
+// (lane's best untaken logit, warp max by key, warp min of the index among the
+// lanes holding it); lanes scan experts lane, lane+32, ... so ties resolve to
+// the lower index.  chosen[j], cv[j]: expert and logit of rank j, every lane.
+__device__ void row_topk(const float* l, int E, int k, int lane, int* chosen, float* cv) {
   if (E <= 16 * 32) {  // the lane's logits (experts lane, lane + 32, ...) held in registers
     float vb[16];
 #pragma unroll
@@ -186,8 +186,7 @@ __global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, i
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const float v = vb[q];
-        const uint32_t ub = __float_as_uint(v == 0.0f ? 0.0f : v);
-        const uint32_t key = (ub & 0x80000000u) ? ~ub : (ub | 0x80000000u);
+        const uint32_t key = logit_key(v);
         if (q * 32 + lane < E && !((taken >> q) & 1u) && (bq < 0 || key > best)) {  // ascending e: ties keep the lower
           best = key;
           bv = v;
@@ -201,17 +200,16 @@ __global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, i
       chosen[j] = win;
       cv[j] = __shfl_sync(0xffffffffu, bv, win & 31);
     }
+    return;
   }
-  for (int j = 0; j < k && E > 16 * 32; ++j) {
+  for (int j = 0; j < k; ++j) {
     uint32_t best = 0u;
     int bi = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
       bool taken = false;
       for (int q = 0; q < j; ++q) taken |= chosen[q] == e;
       if (taken) continue;
-      const float v = l[e];
-      const uint32_t ub = __float_as_uint(v == 0.0f ? 0.0f : v);
-      const uint32_t key = (ub & 0x80000000u) ? ~ub : (ub | 0x80000000u);
+      const uint32_t key = logit_key(l[e]);
       if (bi == 0x7fffffff || key > best) {  // ascending e: ties keep the lower index
         best = key;
         bi = e;
@@ -223,17 +221,304 @@ __global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, i
     chosen[j] = win;
     cv[j] = l[win];
   }
-  if (lane == 0) {
-    float ex[kMaxTopK];
-    float z = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      ex[j] = expf(cv[j] - cv[0]);
-      z += ex[j];
+}
+
+// Lane 0: the token's experts and their weights, the softmax of the k chosen
+// logits renormalised over the k.
+__device__ __forceinline__ void write_routing(int64_t t, int k, int lane, const int* chosen, const float* cv,
+                                              int32_t* idx, float* wout) {
+  if (lane != 0) return;
+  float ex[kMaxTopK];
+  float z = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    ex[j] = expf(cv[j] - cv[0]);
+    z += ex[j];
+  }
+  for (int j = 0; j < k; ++j) {
+    idx[t * k + j] = chosen[j];
+    wout[t * k + j] = ex[j] / z;
+  }
+}
+
+// One warp per token: top-k of the exact logit row, then the weights.
+__global__ void pf_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                               int32_t* __restrict__ idx, float* __restrict__ wout) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int chosen[kMaxTopK];
+  float cv[kMaxTopK];
+  row_topk(logits + (int64_t)t * E, E, k, lane, chosen, cv);
+  write_routing(t, k, lane, chosen, cv, idx, wout);
+}
+
+// ------------------------------------------------------------------ bounded router
+// Routing with the router logits on tensor cores.  A bf16 GEMM (cuBLAS, fp32
+// accumulation, any internal order) gives approximate logits a[t][e]; the
+// top-k must be that of the library's fixed-order fp32 logits F[t][e] (the
+// order of pf_router_kernel), so a rigorous bound |a + b_e - F| <= d[t][e]
+// decides which experts can still be among the k largest F, and only those
+// are recomputed in the fixed order.
+//
+// The bound.  Every product x_i w_i of two bf16 values is exact in fp32.  An
+// fp32 accumulation that adds blocks of n products to a running sum, aligning
+// the n + 1 terms to the largest exponent and dropping the bits below it (no
+// guard bits, truncation: the weakest tensor-core adder model), errs per
+// block by less than (n + 1) ulp of its largest term, so over H / n blocks by
+// less than H (n + 1) / n 2^-23 sum|x_i w_i| <= H 2^-22 sum|x_i w_i|; the
+// fixed-order sum (chains of H / 32 fmas and five butterfly adds, round to
+// nearest) errs by at most (H / 32 + 5) 2^-24 sum|x_i w_i|; adding the bias on
+// either side rounds once more (2^-24 of |a| + |b|).  With
+// sum|x_i w_i| <= ||x|| ||w|| (Cauchy-Schwarz),
+//     d[t][e] = H 2^-20 ||x_t|| ||w_e|| + 2^-21 |b_e| + 2^-100
+// (norms rounded up, products and sums rounded up) is four times the sum of
+// those terms; the 2^-100 covers products flushed to zero on the tensor cores.
+// With lo = a + b - d, hi = a + b + d (rounded down / up) and tau the k-th
+// largest lo, an expert with hi < tau lies strictly below k experts whose
+// F >= lo >= tau, so it is not among the k largest nor tied with them; the
+// rest (the candidates, at least k) get their fixed-order logit, and the k
+// rounds of the top-k over the candidates take exactly the choices the rounds
+// over all E would.  A token whose bounds are not all finite and below 1e37,
+// or with more than kCand candidates, has all E logits recomputed.
+
+constexpr int kCand = 64;  // candidates per token held by the warp (two per lane)
+
+// Upper bound of the 2-norm of a bf16 row of length H (H a multiple of 256), one warp.
+__device__ __forceinline__ float row_norm_ru(const uint16_t* __restrict__ r, int H, int lane) {
+  float s = 0.0f;
+  for (int c = lane * 8; c < H; c += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(r + c));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xffff0000u);
+      s = __fmaf_ru(lo, lo, s);
+      s = __fmaf_ru(hi, hi, s);
     }
-    for (int j = 0; j < k; ++j) {
-      idx[(int64_t)t * k + j] = chosen[j];
-      wout[(int64_t)t * k + j] = ex[j] / z;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) s = __fadd_ru(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return __fsqrt_ru(s);
+}
+
+__global__ void __launch_bounds__(256) router_norm_kernel(const uint16_t* __restrict__ wr, int E, int H,
+                                                          float* __restrict__ out) {
+  const int lane = threadIdx.x & 31, e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const float v = row_norm_ru(wr + (int64_t)e * H, H, lane);
+  if (lane == 0) out[e] = v;
+}
+
+// Fixed-order router logits of experts e4[0..3] for the token row xr: lane j
+// accumulates elements 256m + 8j + r (m, then r ascending) with one rounding
+// per fma, the xor butterfly, then the bias -- the arithmetic of
+// pf_router_kernel, so the results are the same bits.
+__device__ __forceinline__ void exact_logits4(const uint16_t* __restrict__ xr, const uint16_t* __restrict__ wr,
+                                              const float* __restrict__ bias, int H, int lane, const int (&e4)[4],
+                                              float (&v4)[4]) {
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int c = lane * 8; c < H; c += 256) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + c));
+    uint4 wv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wv[j] = __ldg(reinterpret_cast<const uint4*>(wr + (int64_t)e4[j] * H + c));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j] = fma_bf16_lo(xv.x, wv[j].x, acc[j]);
+      acc[j] = fma_bf16_hi(xv.x, wv[j].x, acc[j]);
+      acc[j] = fma_bf16_lo(xv.y, wv[j].y, acc[j]);
+      acc[j] = fma_bf16_hi(xv.y, wv[j].y, acc[j]);
+      acc[j] = fma_bf16_lo(xv.z, wv[j].z, acc[j]);
+      acc[j] = fma_bf16_hi(xv.z, wv[j].z, acc[j]);
+      acc[j] = fma_bf16_lo(xv.w, wv[j].w, acc[j]);
+      acc[j] = fma_bf16_hi(xv.w, wv[j].w, acc[j]);
     }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float v = acc[j];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
+    v4[j] = v + bias[e4[j]];
+  }
+}
+
+// One warp per token.  NQ > 0: the lane's bounds (experts lane, lane + 32, ...)
+// held in registers, E <= 32 NQ; NQ = 0: recomputed from memory (any E).
+// lg [T][E] holds the approximate dot products on entry (the bias not yet
+// added); rows of tokens that take the full path are overwritten with their
+// exact logits.  exact_count += fixed-order logits computed.
+template <int NQ>
+__global__ void __launch_bounds__(256) pf_select_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                                        const uint16_t* __restrict__ wr,
+                                                        const float* __restrict__ bias,
+                                                        const float* __restrict__ wnorm, int E, int k,
+                                                        float* __restrict__ lg, int32_t* __restrict__ idx,
+                                                        float* __restrict__ wout,
+                                                        unsigned long long* __restrict__ exact_count) {
+  __shared__ int cand_e[8][kCand];
+  __shared__ float cand_v[8][kCand];
+  __shared__ int nexact[8];
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + wp;
+  if (lane == 0) nexact[wp] = 0;
+  if (t < T) {
+    const uint16_t* xr = x + (int64_t)t * H;
+    float* row = lg + (int64_t)t * E;
+    const float nx = row_norm_ru(xr, H, lane);
+    const float dx = __fmul_ru((float)H * 0x1p-20f, nx);
+    auto bounds = [&](int e, float& lo, float& hi) -> bool {
+      const float b = bias[e], nw = wnorm[e];
+      const float a = row[e] + b;
+      const float d = __fmaf_ru(dx, nw, __fmaf_ru(0x1p-21f, fabsf(b), 0x1p-100f));
+      lo = __fsub_rd(a, d);
+      hi = __fadd_ru(a, d);
+      return __fmul_ru(nx, nw) < 1e37f && fabsf(b) < 1e37f && fabsf(a) < 1e37f && d < 1e37f;
+    };
+    constexpr bool R = NQ > 0;
+    float lo_r[R ? NQ : 1], hi_r[R ? NQ : 1];
+    bool ok = true;
+    if constexpr (R) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        lo_r[q] = hi_r[q] = 0.0f;
+        if (q * 32 + lane < E) ok &= bounds(q * 32 + lane, lo_r[q], hi_r[q]);
+      }
+    } else {
+      for (int e = lane; e < E; e += 32) {
+        float lo, hi;
+        ok &= bounds(e, lo, hi);
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    int n = kCand + 1;  // candidates; > kCand: the full path
+    if (ok) {
+      // tau = the k-th largest lo, counted with multiplicity: rounds of (largest
+      // key below the previous round's, how many experts hold it)
+      uint32_t cur = 0xffffffffu, tau = 0u;
+      int need = k;
+      for (int r = 0; r < k; ++r) {
+        uint32_t best = 0u;
+        if constexpr (R) {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            const uint32_t key = logit_key(lo_r[q]);
+            if (q * 32 + lane < E && key < cur && key > best) best = key;
+          }
+        } else {
+          for (int e = lane; e < E; e += 32) {
+            float lo, hi;
+            bounds(e, lo, hi);
+            const uint32_t key = logit_key(lo);
+            if (key < cur && key > best) best = key;
+          }
+        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+        uint32_t c = 0;
+        if constexpr (R) {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) c += (q * 32 + lane < E && logit_key(lo_r[q]) == m) ? 1u : 0u;
+        } else {
+          for (int e = lane; e < E; e += 32) {
+            float lo, hi;
+            bounds(e, lo, hi);
+            c += logit_key(lo) == m ? 1u : 0u;
+          }
+        }
+        c = __reduce_add_sync(0xffffffffu, c);
+        tau = m;
+        if ((int)c >= need) break;
+        need -= (int)c;
+        cur = m;
+      }
+      // candidates hi >= tau, in ascending expert order
+      n = 0;
+      const int nq = R ? NQ : (E + 31) / 32;
+#pragma unroll
+      for (int q = 0; q < nq; ++q) {
+        const int e = q * 32 + lane;
+        float hi = 0.0f;
+        if constexpr (R) {
+          hi = hi_r[q];
+        } else if (e < E) {
+          float lo;
+          bounds(e, lo, hi);
+        }
+        const bool in = e < E && logit_key(hi) >= tau;
+        const uint32_t bal = __ballot_sync(0xffffffffu, in);
+        const int pos = n + __popc(bal & ((1u << lane) - 1u));
+        if (in && pos < kCand) cand_e[wp][pos] = e;
+        n += __popc(bal);
+      }
+      if (n < k) n = kCand + 1;  // cannot happen (the k experts defining tau are candidates)
+    }
+    __syncwarp();
+    int chosen[kMaxTopK];
+    float cv[kMaxTopK];
+    if (n <= kCand) {
+      for (int c = 0; c < n; c += 4) {
+        int e4[4];
+        float v4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e4[j] = cand_e[wp][min(c + j, n - 1)];
+        exact_logits4(xr, wr, bias, H, lane, e4, v4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (lane == j && c + j < n) cand_v[wp][c + j] = v4[j];
+      }
+      __syncwarp();
+      // top-k over the candidates (slot lane, then lane + 32: ascending expert)
+      const bool h0 = lane < n, h1 = lane + 32 < n;
+      const int e0 = h0 ? cand_e[wp][lane] : 0, e1 = h1 ? cand_e[wp][lane + 32] : 0;
+      const float v0 = h0 ? cand_v[wp][lane] : 0.0f, v1 = h1 ? cand_v[wp][lane + 32] : 0.0f;
+      bool tk0 = false, tk1 = false;
+      for (int j = 0; j < k; ++j) {
+        uint32_t best = 0u;
+        int be = -1, bs = 0;
+        float bv = 0.0f;
+        if (h0 && !tk0) {
+          best = logit_key(v0);
+          be = e0;
+          bv = v0;
+        }
+        if (h1 && !tk1 && (be < 0 || logit_key(v1) > best)) {  // ties keep the lower expert
+          best = logit_key(v1);
+          be = e1;
+          bv = v1;
+          bs = 1;
+        }
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, be < 0 ? 0u : best);
+        const uint32_t mine = (be >= 0 && best == kmax) ? (uint32_t)be : 0xffffffffu;
+        const int win = (int)__reduce_min_sync(0xffffffffu, mine);
+        const bool own = be >= 0 && be == win;
+        if (own) (bs ? tk1 : tk0) = true;
+        const int wl = __ffs(__ballot_sync(0xffffffffu, own)) - 1;
+        chosen[j] = win;
+        cv[j] = __shfl_sync(0xffffffffu, bv, wl);
+      }
+    } else {  // the full path: every logit in the fixed order, then the plain top-k
+      n = E;
+      for (int c = 0; c < E; c += 4) {
+        int e4[4];
+        float v4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e4[j] = min(c + j, E - 1);
+        exact_logits4(xr, wr, bias, H, lane, e4, v4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (lane == j && c + j < E) row[c + j] = v4[j];
+      }
+      __syncwarp();
+      row_topk(row, E, k, lane, chosen, cv);
+    }
+    write_routing(t, k, lane, chosen, cv, idx, wout);
+    if (lane == 0) nexact[wp] = n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long s = 0;
+    for (int w = 0; w < 8; ++w) s += (unsigned long long)nexact[w];
+    atomicAdd(exact_count, s);
   }
 }
 
@@ -901,7 +1186,7 @@ __global__ void pf_stats_kernel(const int32_t* __restrict__ counts, int E, const
                                 unsigned long long* stats, int64_t expert_bytes, int64_t router_bytes,
                                 int n_pairs, int lfu, int64_t ge0, uint32_t* lfu_count, int32_t* lfu_last,
                                 const int* step, int32_t* miss_list, unsigned* miss_count, int miss_cap,
-                                uint32_t* overflow) {
+                                uint32_t* overflow, unsigned long long exact_all) {
   __shared__ int sh[2];
   if (threadIdx.x == 0) sh[0] = sh[1] = 0;
   __syncthreads();
@@ -930,6 +1215,7 @@ __global__ void pf_stats_kernel(const int32_t* __restrict__ counts, int E, const
     stats[kStatHostBytes] += (D - hits) * (unsigned long long)expert_bytes;
     stats[kStatPairs] += (unsigned long long)n_pairs;
     stats[kStatForwards] += 1ull;
+    stats[kStatRouterExact] += exact_all;
   }
 }
 
@@ -1007,6 +1293,11 @@ size_t gemm_smem(const GemmArgs& a, int E) {
 
 }  // namespace
 
+cudaError_t moe::router_norms(const uint16_t* wr, int E, int H, float* out, cudaStream_t s) {
+  router_norm_kernel<<<(E + 7) / 8, 256, 0, s>>>(wr, E, H, out);
+  return cudaGetLastError();
+}
+
 cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
                                  cudaStream_t s, const moe_routing_out* dbg, bool lfu,
                                  const uint8_t* const* blob_hbm) {
@@ -1014,12 +1305,29 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
   const int E = d.num_experts, H = d.hidden, I = d.inter, k = d.top_k;
   const int n = T * k;
   cudaError_t e;
-  {
+  unsigned long long* st = p.stats + (int64_t)layer * kNumStats;
+  const bool all_logits = dbg && dbg->logits;
+  if (all_logits) {  // every logit in the fixed order (the caller reads them)
     const dim3 grid((T + kRtTok - 1) / kRtTok, (E + kRtExp - 1) / kRtExp);
     if ((e = ensure_dynamic_smem((const void*)pf_router_kernel, kRtSmem)) != cudaSuccess) return e;
     pf_router_kernel<<<grid, 256, kRtSmem, s>>>(x, T, H, p.wr[layer], p.bias[layer], E, p.logits);
+    pf_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(p.logits, T, E, k, p.topk_idx, p.topk_w);
+  } else {  // bounded tensor-core logits, then the fixed order for the candidates only
+    const float one = 1.0f, zero = 0.0f;
+    if (cublasSetStream(p.blas, s) != CUBLAS_STATUS_SUCCESS ||
+        cublasGemmEx(p.blas, CUBLAS_OP_T, CUBLAS_OP_N, E, T, H, &one, p.wr[layer], CUDA_R_16BF, H, x,
+                     CUDA_R_16BF, H, &zero, p.logits, CUDA_R_32F, E, CUBLAS_COMPUTE_32F,
+                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return cudaErrorLaunchFailure;
+    if (E <= 16 * 32)
+      pf_select_kernel<16><<<(T + 7) / 8, 256, 0, s>>>(x, T, H, p.wr[layer], p.bias[layer],
+                                                       p.wnorm_all + (int64_t)layer * E, E, k, p.logits,
+                                                       p.topk_idx, p.topk_w, st + kStatRouterExact);
+    else
+      pf_select_kernel<0><<<(T + 7) / 8, 256, 0, s>>>(x, T, H, p.wr[layer], p.bias[layer],
+                                                      p.wnorm_all + (int64_t)layer * E, E, k, p.logits,
+                                                      p.topk_idx, p.topk_w, st + kStatRouterExact);
   }
-  pf_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(p.logits, T, E, k, p.topk_idx, p.topk_w);
   {
     const int nb = (n + kGroupChunk - 1) / kGroupChunk;
     const size_t hsm = (size_t)E * 4, wsm = (size_t)8 * E * 4;
@@ -1089,11 +1397,11 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     if ((e = launch_gemm<false>(d.weight_bits, map, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
   pf_combine_kernel<<<4 * p.sms, 256, 0, s>>>(p.pf_o, p.inv, T, H, k, y);
-  pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, bhbm, p.stats + (int64_t)layer * kNumStats,
+  pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, bhbm, st,
                                     p.lay.algo_bytes, (int64_t)E * H * 2, n,
                                     lfu && d.cache_policy == MOE_POLICY_LFU, ge0, p.lfu_count, p.lfu_last,
                                     &p.ctl->step, p.miss_list, p.miss_count, d.num_layers * p.max_distinct,
-                                    p.err_dev + 1);
+                                    p.err_dev + 1, all_logits ? (unsigned long long)T * E : 0ull);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (dbg) {  // optional routing outputs
     if (dbg->logits) cudaMemcpyAsync(dbg->logits, p.logits, (size_t)T * E * 4, cudaMemcpyDeviceToDevice, s);

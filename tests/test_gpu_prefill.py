@@ -28,19 +28,23 @@ def _oracle_expert(wl, layer, e):
     return oracle.QuantExpert([c for c, _ in q], [s for _, s in q])
 
 
-def _run(plan, x_bits, wl):
+def _run(plan, x_bits, wl, logits=True):
+    """One forward with the routing outputs.  Asking for the logits makes the
+    library compute every logit in its fixed order; without them the routing
+    takes the bounded tensor-core pass."""
     import torch
     T = x_bits.shape[0]
     x = torch.from_numpy(x_bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
     y = torch.empty_like(x)
     E, k = wl.experts, wl.top_k
-    dbg = dict(logits=torch.empty(T, E, dtype=torch.float32, device="cuda"),
-               topk_idx=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+    dbg = dict(topk_idx=torch.empty(T, k, dtype=torch.int32, device="cuda"),
                topk_w=torch.empty(T, k, dtype=torch.float32, device="cuda"),
                counts=torch.empty(E, dtype=torch.int32, device="cuda"),
                offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
                perm=torch.empty(T * k, dtype=torch.int32, device="cuda"),
                inv=torch.empty(T * k, dtype=torch.int32, device="cuda"))
+    if logits:
+        dbg["logits"] = torch.empty(T, E, dtype=torch.float32, device="cuda")
     plan.forward(0, x, y, dbg=dbg)
     torch.cuda.synchronize()
     yb = oracle.bf16_to_f32(y.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
