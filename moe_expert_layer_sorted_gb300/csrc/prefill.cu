@@ -817,7 +817,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // dynamic window (1024-aligned for the swizzled tiles): token ring | weight
   // ring | code-block ring (codes of the 16 tiles, then their scales) | unit table
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  // (offset from the array itself, so that every derived pointer stays a shared-space one)
+  uint8_t* smem = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
   uint8_t* tokr = smem;
   uint8_t* wr = tokr + (size_t)a.nt * kTokBytes;
   const uint32_t kbBytes = kItems * (a.kb_codes + a.kb_scales);
