@@ -628,29 +628,53 @@ __global__ void __launch_bounds__(256) pf_bucket_place(const int32_t* __restrict
 
 // ------------------------------------------------------------------ token rows in (expert, token) order
 
-// xp[p] = x[perm[p] / k]: the layer input gathered into the grouped order, so
-// that every GEMM unit's token rows are one contiguous tile for the TMA.  One
-// warp per row: one perm lookup, then the row's 16-byte pieces, up to 16 per
-// lane in flight.
+// K order of the GEMM operands within each 64-column stage.  Word w (columns
+// 2w, 2w+1) of a stage's half h (columns 32h..32h+31) is written as
+// w = 8 kk1 + 4 m + j with j < 4, kk1, m < 2 -- MMA step 2h + kk1 and, within
+// the step, columns 2j + 8m, 2j + 8m + 1; it is placed at physical word
+// 8 j + 4 h + 2 kk1 + m of the stage.  So physical 16-byte chunk 2j + h holds
+// exactly what dequantising lane j (tig = j) produces for its row in MMA steps
+// 2h and 2h+1 (its mma.m16n8k16 A-fragment columns), one 16-byte store, and a
+// quarter warp's eight stores hit eight different chunks of the swizzled rows.
+// The token rows (pf_gather_kernel) and h (the gate/up epilogue, the down
+// GEMM's token operand) take the same order, so every product pairs the same
+// column of both operands.  In words of one half: a 4 x 4 transpose, chunk
+// 2j + h = (word j, j + 4, j + 8, j + 12).
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// xp[p] = x[perm[p] / k] with its columns in the stage order above: the layer
+// input gathered into the grouped order, so that every GEMM unit's token rows
+// are one contiguous tile for the TMA.  One warp per row: one perm lookup,
+// then the row's 128-byte stages, up to two per lane in flight.
 __global__ void __launch_bounds__(256) pf_gather_kernel(const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ perm, int n, int k, int H,
                                                         uint16_t* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
-  const int per = H / 8;  // 16-byte pieces per row
+  const int per = H / 64;  // 64-column stages per row
   for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n; p += gridDim.x * (blockDim.x >> 5)) {
-    const uint4* src = reinterpret_cast<const uint4*>(x) + (int64_t)(perm[p] / k) * per;
-    uint4* dst = reinterpret_cast<uint4*>(xp) + (int64_t)p * per;
-    for (int c0 = 0; c0 < per; c0 += 16 * 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(x) + (int64_t)(perm[p] / k) * per * 8;
+    uint4* dst = reinterpret_cast<uint4*>(xp) + (int64_t)p * per * 8;
+    for (int c0 = 0; c0 < per; c0 += 2 * 32) {
       uint4 v[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const int c = c0 + q * 32 + lane;
-        if (c < per) v[q] = src[c];
+        if (c < per)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[8 * q + i] = src[8 * c + i];
       }
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const int c = c0 + q * 32 + lane;
-        if (c < per) dst[c] = v[q];
+        if (c < per)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[8 * c + 2 * j + h] = make_uint4(word_of(v[8 * q + 4 * h], j), word_of(v[8 * q + 4 * h + 1], j),
+                                                  word_of(v[8 * q + 4 * h + 2], j), word_of(v[8 * q + 4 * h + 3], j));
       }
     }
   }
@@ -800,6 +824,103 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Shared-memory rings the dequantising warps use.
+struct DqRings {
+  uint8_t* kbr;  // code-block ring: per slot the 16 tiles' codes, then their scales
+  uint32_t kbBytes;
+  uint8_t* wr;  // weight ring: per slot 256 dequantised rows x 64 columns, swizzled
+  unsigned long long *kbFull, *kbEmpty, *wFull, *wEmpty;
+};
+
+// Scale of row r of a 16-row group record (16 scales of SDT).
+template <int SDT>
+__device__ __forceinline__ float scale_of(const uint8_t* rec, int r) {
+  if constexpr (SDT == MOE_SCALE_F32) return reinterpret_cast<const float*>(rec)[r];
+  else if constexpr (SDT == MOE_SCALE_BF16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(rec)[r] << 16);
+  else return __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(rec)[r]));
+}
+
+// Dequantising warp w: its 16-row tile (rows 16w..16w+15 of the unit's 256)
+// of every stage, codes and scales from the code-block ring, into bf16 s*q in
+// the weight ring, 128-byte-swizzled K-major in the stage K order (see
+// pf_gather_kernel).  One code block (256 columns, four stages) per iteration:
+// the block's wait and release once, the stages unrolled.
+template <int B, int SDT>
+__device__ __forceinline__ void dequant_tiles(const GemmArgs& a, const DqRings& r, int nunits, int S, int warp,
+                                              int lane) {
+  const int g = lane >> 2, tig = lane & 3;
+  // the lane's elements of a row in MMA steps 2h and 2h+1 are chunk 2tig + h;
+  // swizzled offsets in rows g, g+8
+  const uint32_t offh0 = (uint32_t)(((2 * tig) ^ (g & 7)) << 4), offh1 = (uint32_t)(((2 * tig + 1) ^ (g & 7)) << 4);
+  constexpr int ssz = SDT == MOE_SCALE_F32 ? 4 : 2;
+  const float zb = 128.0f + (float)(1 << (B - 1));
+  const uint32_t negzb2 = pack_bf16x2(-zb, -zb);  // exact: 130, 132 or 136
+  const int lg_g = 31 - __clz(a.G);                // G = 32, 64 or 128
+  RingPos kp, wp;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      const int nq = min(4, S - s0);
+      const int kslot = kp.slot;
+      mbar_wait(smem_addr(&r.kbFull[kslot]), kp.phase, a.err);
+      const uint8_t* kb = r.kbr + (size_t)kslot * r.kbBytes;
+      const uint8_t* citem = kb + warp * a.kb_codes;
+      const uint8_t* sitem = kb + kItems * a.kb_codes + warp * a.kb_scales;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q < nq) {
+          const int wslot = wp.slot;
+          mbar_wait(smem_addr(&r.wEmpty[wslot]), wp.phase ^ 1u, a.err);
+          uint32_t w[4];
+          chunk_words<B>(citem, lane, q, w);
+          float sc[4];  // rows g, g+8 of the stage's column halves 0 and 1
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t* rec = sitem + ((q * 64 + 32 * h) >> lg_g) * (16 * ssz);
+            sc[2 * h] = scale_of<SDT>(rec, g);
+            sc[2 * h + 1] = scale_of<SDT>(rec, g + 8);
+          }
+          uint32_t out[16];  // pair i: MMA step i/4 of the stage, fragment register i%4
+          if constexpr (SDT == MOE_SCALE_BF16) {  // (128 + u) - zb is exact in bf16; one rounding for the product
+            uint32_t s2[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) s2[h] = pack_bf16x2(sc[h], sc[h]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t v = chunk_pair<B>(w, i);
+              const int kk = i >> 2, rr = i & 3;
+              uint32_t t;
+              asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(v), "r"(0x3F803F80u), "r"(negzb2));
+              asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(t), "r"(s2[(kk >= 2 ? 2 : 0) + (rr & 1)]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t v = chunk_pair<B>(w, i);
+              const int kk = i >> 2, rr = i & 3;
+              const float sv = sc[(kk >= 2 ? 2 : 0) + (rr & 1)];
+              out[i] = pack_bf16x2((bf16f(v & 0xffffu) - zb) * sv, (__uint_as_float(v & 0xffff0000u) - zb) * sv);
+            }
+          }
+          uint8_t* r0 = r.wr + (size_t)wslot * kWBytes + (warp * 16 + g) * 128;
+          uint8_t* r1 = r0 + 8 * 128;
+          *reinterpret_cast<uint4*>(r0 + offh0) = make_uint4(out[0], out[2], out[4], out[6]);
+          *reinterpret_cast<uint4*>(r1 + offh0) = make_uint4(out[1], out[3], out[5], out[7]);
+          *reinterpret_cast<uint4*>(r0 + offh1) = make_uint4(out[8], out[10], out[12], out[14]);
+          *reinterpret_cast<uint4*>(r1 + offh1) = make_uint4(out[9], out[11], out[13], out[15]);
+          // every lane's stores visible to the tensor core, then one arrival for the warp
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&r.wFull[wslot]));
+          wp.next(a.nw);
+        }
+      }
+      // the warp reads the code block no more
+      if (lane == 0) mbar_arrive(smem_addr(&r.kbEmpty[kslot]));
+      kp.next(a.nkbs);
+    }
+  }
+}
+
 // Grouped dequant-GEMM over units (expert e, 128 of its tokens, 256 weight rows):
 // D[token][row] = sum_k xg[token][k] * s * q[row][k], the token rows (A, M = 128)
 // a tile of the grouped activations by tensor copy, the weight rows (B, N = 256)
@@ -893,72 +1014,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
 
   if (warp < kDqWarps) {
     // ------------------------------------------------------------ dequantisers
-    // Warp w turns its 16-row tile of each stage (codes and scales from the
-    // code-block ring) into bf16 s*q, 128-byte-swizzled K-major, in the
-    // weight ring: rows 16w..16w+15 of the unit's 256.
-    const int g = lane >> 2, tig = lane & 3;
-    uint32_t offc[8];  // swizzled byte offset of the lane's 4 bytes in 16-byte chunk c of rows g, g+8
-#pragma unroll
-    for (int c = 0; c < 8; ++c) offc[c] = (uint32_t)(((c ^ (g & 7)) << 4) + 4 * tig);
-    const bool bfs = a.sdt == MOE_SCALE_BF16;
-    const int ssz = a.sdt == MOE_SCALE_F32 ? 4 : 2;
-    const float zb = 128.0f + (float)(1 << (B - 1));
-    const uint32_t negzb2 = pack_bf16x2(-zb, -zb);  // exact: 130, 132 or 136
-    const int lg_g = 31 - __clz(a.G);                      // G = 32, 64 or 128
-    const int lg_srow = ssz == 4 ? 6 : 5;                  // bytes of 16 scales = 1 << lg_srow
-    RingPos kp, wp;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-      for (int s = 0; s < S; ++s) {
-        const int q = s & 3, kslot = kp.slot, wslot = wp.slot;
-        if (q == 0) mbar_wait(smem_addr(&kbFull[kslot]), kp.phase, a.err);
-        mbar_wait(smem_addr(&wEmpty[wslot]), wp.phase ^ 1u, a.err);
-        const uint8_t* kb = kbr + (size_t)kslot * kbBytes;
-        uint32_t w[4];
-        chunk_words<B>(kb + warp * a.kb_codes, lane, q, w);
-        const uint8_t* sitem = kb + kItems * a.kb_codes + warp * a.kb_scales;
-        float sc[4];  // rows g, g+8 of the stage's column halves 0 and 1
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint8_t* srow = sitem + (((q * 64 + 32 * h) >> lg_g) << lg_srow);
-          sc[2 * h] = scale_at(srow, g, a.sdt);
-          sc[2 * h + 1] = scale_at(srow, g + 8, a.sdt);
-        }
-        uint8_t* r0 = wr + (size_t)wslot * kWBytes + (warp * 16 + g) * 128;
-        uint8_t* r1 = r0 + 8 * 128;
-        if (bfs) {  // (128 + u) - zb is exact in bf16; one rounding for the product
-          uint32_t s2[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) s2[h] = pack_bf16x2(sc[h], sc[h]);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {  // pair i: k-step i/4 of the stage, register i%4
-            const uint32_t v = chunk_pair<B>(w, i);
-            const int kk = i >> 2, r = i & 3;
-            uint32_t t, out;
-            asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(v), "r"(0x3F803F80u), "r"(negzb2));
-            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(t), "r"(s2[(kk >= 2 ? 2 : 0) + (r & 1)]));
-            *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t v = chunk_pair<B>(w, i);
-            const int kk = i >> 2, r = i & 3;
-            const float sv = sc[(kk >= 2 ? 2 : 0) + (r & 1)];
-            const uint32_t out = pack_bf16x2((bf16f(v & 0xffffu) - zb) * sv, (__uint_as_float(v & 0xffff0000u) - zb) * sv);
-            *reinterpret_cast<uint32_t*>(((r & 1) ? r1 : r0) + offc[2 * kk + (r >> 1)]) = out;
-          }
-        }
-        // every lane's stores visible to the tensor core, then one arrival for the warp
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&wFull[wslot]));
-        if (q == 3 || s == S - 1) {  // the warp reads the code block no more
-          if (lane == 0) mbar_arrive(smem_addr(&kbEmpty[kslot]));
-          kp.next(a.nkbs);
-        }
-        wp.next(a.nw);
-      }
-    }
+    const DqRings r{kbr, kbBytes, wr, kbFull, kbEmpty, wFull, wEmpty};
+    if (a.sdt == MOE_SCALE_BF16) dequant_tiles<B, MOE_SCALE_BF16>(a, r, nunits, S, warp, lane);
+    else if (a.sdt == MOE_SCALE_F16) dequant_tiles<B, MOE_SCALE_F16>(a, r, nunits, S, warp, lane);
+    else dequant_tiles<B, MOE_SCALE_F32>(a, r, nunits, S, warp, lane);
   } else if (warp == kKbWarp) {
     // ------------------------------------------------------------ code blocks
     // Per 256-column code block (4 stages) of a unit: the 16 tiles' codes and
@@ -1092,23 +1151,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
       uint16_t* orow = a.out + (int64_t)(n0 + row) * a.out_ld;
       if constexpr (GATEUP) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-          uint32_t gv[16], uv[16];
-          tmem_ld16_nowait(ta + c0, gv);
-          tmem_ld16_nowait(ta + 128 + c0, uv);
-          tmem_wait_ld();
-          uint32_t hp[8];
+        for (int c0 = 0; c0 < 128; c0 += 32) {  // half (c0 / 32) & 1 of a 64-column stage of h
+          uint32_t hp[16];                      // words of the 32 columns, column order
 #pragma unroll
-          for (int c = 0; c < 16; c += 2) {
-            const float g0 = __uint_as_float(gv[c]), g1 = __uint_as_float(gv[c + 1]);
-            const float h0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(uv[c]);
-            const float h1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(uv[c + 1]);
-            hp[c >> 1] = pack_bf16x2(h0, h1);
+          for (int kk1 = 0; kk1 < 2; ++kk1) {
+            uint32_t gv[16], uv[16];
+            tmem_ld16_nowait(ta + c0 + 16 * kk1, gv);
+            tmem_ld16_nowait(ta + 128 + c0 + 16 * kk1, uv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; c += 2) {
+              const float g0 = __uint_as_float(gv[c]), g1 = __uint_as_float(gv[c + 1]);
+              const float h0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(uv[c]);
+              const float h1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(uv[c + 1]);
+              hp[8 * kk1 + (c >> 1)] = pack_bf16x2(h0, h1);
+            }
           }
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + rt * 128 + c0);
-            dst[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            dst[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+          if (live) {  // h in the stage K order (pf_gather_kernel): the down GEMM's token operand
+            uint4* dst = reinterpret_cast<uint4*>(orow + rt * 128 + (c0 & ~63));
+            const int h = (c0 >> 5) & 1;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[2 * j + h] = make_uint4(hp[j], hp[j + 4], hp[j + 8], hp[j + 12]);
           }
         }
       } else {
