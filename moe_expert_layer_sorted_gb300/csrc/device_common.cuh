@@ -46,17 +46,30 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// Bounded wait for phase `parity` of bar: ~2^20 tries with a 1 us suspend
-// hint; latches a timeout (and gives up at once once one is latched).
+// Bounded wait for phase `parity` of bar: ~2^20 tries, each suspending the
+// thread until the phase completes or a time limit passes -- a 1 us hint, or
+// (kHint false) the system's own limit, which measured about as long and wakes
+// the thread sooner after the phase completes (the prefill GEMM's pipeline runs
+// a few percent faster with it); latches a timeout (and gives up at once once
+// one is latched).
+template <bool kHint = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
   for (uint32_t it = 0; it < (1u << 20); ++it) {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (kHint)
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
+          " selp.u32 %0, 1, 0, p;\n}"
+          : "=r"(ok)
+          : "r"(bar), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+          " selp.u32 %0, 1, 0, p;\n}"
+          : "=r"(ok)
+          : "r"(bar), "r"(parity)
+          : "memory");
     if (ok) return true;
     if ((it & 255u) == 255u && *reinterpret_cast<volatile uint32_t*>(err)) return false;
   }

@@ -640,42 +640,32 @@ __global__ void __launch_bounds__(256) pf_bucket_place(const int32_t* __restrict
 // GEMM's token operand) take the same order, so every product pairs the same
 // column of both operands.  In words of one half: a 4 x 4 transpose, chunk
 // 2j + h = (word j, j + 4, j + 8, j + 12).
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
-  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-}
 
 // xp[p] = x[perm[p] / k] with its columns in the stage order above: the layer
 // input gathered into the grouped order, so that every GEMM unit's token rows
-// are one contiguous tile for the TMA.  One warp per row: one perm lookup,
-// then the row's 128-byte stages, up to two per lane in flight.
+// are one contiguous tile for the TMA.  One warp per row, 512 bytes (four
+// stages) per round: a coalesced 16-byte load per lane, the 4 x 4 word
+// transposes through shared memory (4 words of padding per 32, so that the
+// transposed reads hit 32 different banks), a coalesced 16-byte store per lane.
 __global__ void __launch_bounds__(256) pf_gather_kernel(const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ perm, int n, int k, int H,
                                                         uint16_t* __restrict__ xp) {
-  const int lane = threadIdx.x & 31;
-  const int per = H / 64;  // 64-column stages per row
-  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n; p += gridDim.x * (blockDim.x >> 5)) {
-    const uint4* src = reinterpret_cast<const uint4*>(x) + (int64_t)(perm[p] / k) * per * 8;
-    uint4* dst = reinterpret_cast<uint4*>(xp) + (int64_t)p * per * 8;
-    for (int c0 = 0; c0 < per; c0 += 2 * 32) {
-      uint4 v[16];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int c = c0 + q * 32 + lane;
-        if (c < per)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[8 * q + i] = src[8 * c + i];
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int c = c0 + q * 32 + lane;
-        if (c < per)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[8 * c + 2 * j + h] = make_uint4(word_of(v[8 * q + 4 * h], j), word_of(v[8 * q + 4 * h + 1], j),
-                                                  word_of(v[8 * q + 4 * h + 2], j), word_of(v[8 * q + 4 * h + 3], j));
-      }
+  __shared__ __align__(16) uint32_t tw[8][4 * 36];
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  uint32_t* t = tw[wp];
+  const int per = H / 8;  // 16-byte pieces per row (a multiple of 32: H is a multiple of 256)
+  // this lane's output piece: stage lane / 8, piece o = 2j + h of it = words j of pieces 4h .. 4h+3
+  const int st = lane >> 3, o = lane & 7, j = o >> 1, h = o & 1;
+  auto word_at = [&](int piece, int word) { return t[(st * 8 + piece) * 4 + word + 4 * st]; };
+  for (int p = blockIdx.x * (blockDim.x >> 5) + wp; p < n; p += gridDim.x * (blockDim.x >> 5)) {
+    const uint4* src = reinterpret_cast<const uint4*>(x) + (int64_t)(perm[p] / k) * per;
+    uint4* dst = reinterpret_cast<uint4*>(xp) + (int64_t)p * per;
+    for (int c0 = 0; c0 < per; c0 += 32) {
+      const uint4 v = src[c0 + lane];
+      __syncwarp();
+      *reinterpret_cast<uint4*>(&t[lane * 4 + 4 * (lane >> 3)]) = v;  // word w of the round at w + 4 (w / 32)
+      __syncwarp();
+      dst[c0 + lane] = make_uint4(word_at(4 * h, j), word_at(4 * h + 1, j), word_at(4 * h + 2, j), word_at(4 * h + 3, j));
     }
   }
 }
@@ -861,7 +851,7 @@ __device__ __forceinline__ void dequant_tiles(const GemmArgs& a, const DqRings& 
     for (int s0 = 0; s0 < S; s0 += 4) {
       const int nq = min(4, S - s0);
       const int kslot = kp.slot;
-      mbar_wait(smem_addr(&r.kbFull[kslot]), kp.phase, a.err);
+      mbar_wait<false>(smem_addr(&r.kbFull[kslot]), kp.phase, a.err);
       const uint8_t* kb = r.kbr + (size_t)kslot * r.kbBytes;
       const uint8_t* citem = kb + warp * a.kb_codes;
       const uint8_t* sitem = kb + kItems * a.kb_codes + warp * a.kb_scales;
@@ -869,7 +859,7 @@ __device__ __forceinline__ void dequant_tiles(const GemmArgs& a, const DqRings& 
       for (int q = 0; q < 4; ++q) {
         if (q < nq) {
           const int wslot = wp.slot;
-          mbar_wait(smem_addr(&r.wEmpty[wslot]), wp.phase ^ 1u, a.err);
+          mbar_wait<false>(smem_addr(&r.wEmpty[wslot]), wp.phase ^ 1u, a.err);
           uint32_t w[4];
           chunk_words<B>(citem, lane, q, w);
           float sc[4];  // rows g, g+8 of the stage's column halves 0 and 1
@@ -1037,7 +1027,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
       const uint8_t* blob = host ? a.blob_host[e] : hb;
       for (int kb = 0; kb < nkbu; ++kb) {
         const int slot = kp.slot;
-        mbar_wait(smem_addr(&kbEmpty[slot]), kp.phase ^ 1u, a.err);
+        mbar_wait<false>(smem_addr(&kbEmpty[slot]), kp.phase ^ 1u, a.err);
         uint8_t* dst = kbr + (size_t)slot * kbBytes;
         const uint32_t bar = smem_addr(&kbFull[slot]);
         if (!host) {
@@ -1090,7 +1080,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
         decode_unit(u, e, rt, n0, nrows);
         for (int s = 0; s < S; ++s) {
           const int slot = tp.slot;
-          mbar_wait(smem_addr(&tokEmpty[slot]), tp.phase ^ 1u, a.err);
+          mbar_wait<false>(smem_addr(&tokEmpty[slot]), tp.phase ^ 1u, a.err);
           const uint32_t bar = smem_addr(&tokFull[slot]);
           mbar_arrive_expect_tx(bar, kTokBytes);
           tma_load_2d(smem_addr(tokr + (size_t)slot * kTokBytes), &tok_map, s * kStageK, n0, bar);
@@ -1109,13 +1099,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
       int ui = 0;
       for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
         const int buf = ui & 1;
-        mbar_wait(smem_addr(&tempty[buf]), ((uint32_t)(ui >> 1) & 1u) ^ 1u, a.err);  // accumulator free
+        mbar_wait<false>(smem_addr(&tempty[buf]), ((uint32_t)(ui >> 1) & 1u) ^ 1u, a.err);  // accumulator free
         tc_fence_after();
         const uint32_t dacc = tmem + (uint32_t)(buf * 256);
         for (int s = 0; s < S; ++s) {
           const int ts = tp.slot, wsl = wp.slot;
-          mbar_wait(smem_addr(&tokFull[ts]), tp.phase, a.err);
-          mbar_wait(smem_addr(&wFull[wsl]), wp.phase, a.err);
+          mbar_wait<false>(smem_addr(&tokFull[ts]), tp.phase, a.err);
+          mbar_wait<false>(smem_addr(&wFull[wsl]), wp.phase, a.err);
           tc_fence_after();
           const uint32_t at = smem_addr(tokr + (size_t)ts * kTokBytes);
           const uint32_t bt = smem_addr(wr + (size_t)wsl * kWBytes);
@@ -1145,7 +1135,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
       const bool live = row < nrows;
       float wgt = 0.0f;
       if (!GATEUP && live) wgt = a.topk_w[a.perm[n0 + row]];
-      mbar_wait(smem_addr(&tfull[buf]), (uint32_t)(ui >> 1) & 1u, a.err);
+      mbar_wait<false>(smem_addr(&tfull[buf]), (uint32_t)(ui >> 1) & 1u, a.err);
       tc_fence_after();
       const uint32_t ta = tmem + (uint32_t)(buf * 256) + ((uint32_t)(quad * 32) << 16);
       uint16_t* orow = a.out + (int64_t)(n0 + row) * a.out_ld;
