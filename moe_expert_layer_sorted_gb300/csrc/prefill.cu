@@ -286,6 +286,7 @@ constexpr int kCand = 64;  // candidates per token held by the warp (two per lan
 // Upper bound of the 2-norm of a bf16 row of length H (H a multiple of 256), one warp.
 __device__ __forceinline__ float row_norm_ru(const uint16_t* __restrict__ r, int H, int lane) {
   float s = 0.0f;
+#pragma unroll 4
   for (int c = lane * 8; c < H; c += 256) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(r + c));
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -317,6 +318,7 @@ __device__ __forceinline__ void exact_logits4(const uint16_t* __restrict__ xr, c
                                               const float* __restrict__ bias, int H, int lane, const int (&e4)[4],
                                               float (&v4)[4]) {
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2
   for (int c = lane * 8; c < H; c += 256) {
     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + c));
     uint4 wv[4];
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(256) pf_select_kernel(const uint16_t* __restri
                                                         float* __restrict__ wout,
                                                         unsigned long long* __restrict__ exact_count) {
   __shared__ int cand_e[8][kCand];
-  __shared__ float cand_v[8][kCand];
+  __shared__ float cand_v[8][kCand], cand_h[8][kCand];
   __shared__ int nexact[8];
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
   const int t = blockIdx.x * 8 + wp;
@@ -447,7 +449,10 @@ __global__ void __launch_bounds__(256) pf_select_kernel(const uint16_t* __restri
         const bool in = e < E && logit_key(hi) >= tau;
         const uint32_t bal = __ballot_sync(0xffffffffu, in);
         const int pos = n + __popc(bal & ((1u << lane) - 1u));
-        if (in && pos < kCand) cand_e[wp][pos] = e;
+        if (in && pos < kCand) {
+          cand_e[wp][pos] = e;
+          cand_h[wp][pos] = hi;
+        }
         n += __popc(bal);
       }
       if (n < k) n = kCand + 1;  // cannot happen (the k experts defining tau are candidates)
@@ -455,20 +460,81 @@ __global__ void __launch_bounds__(256) pf_select_kernel(const uint16_t* __restri
     __syncwarp();
     int chosen[kMaxTopK];
     float cv[kMaxTopK];
+    int nev = n;  // fixed-order logits computed for this token
     if (n <= kCand) {
-      for (int c = 0; c < n; c += 4) {
-        int e4[4];
-        float v4[4];
+      // Fixed-order logits in rounds, the candidates with the largest upper
+      // bounds first, until every candidate not computed has an upper bound
+      // below the k-th largest computed logit: such a candidate lies strictly
+      // below k computed experts, so the top-k over the computed ones is the
+      // top-k over all (same choices, same order).  Slots lane and lane + 32.
+      const bool s0 = lane < n, s1 = lane + 32 < n;
+      const uint32_t hk0 = s0 ? logit_key(cand_h[wp][lane]) : 0u;
+      const uint32_t hk1 = s1 ? logit_key(cand_h[wp][lane + 32]) : 0u;
+      uint64_t evm = 0;  // slots computed (the same in every lane)
+      int batch = min(8, (k + 5) & ~3);
+      nev = 0;
+      while (true) {
+        int pick[8];
+        int np = 0;
+        for (int b = 0; b < batch && nev + np < n; ++b) {  // largest bound first, ties: lower slot
+          const bool a0 = s0 && !((evm >> lane) & 1ull), a1 = s1 && !((evm >> (lane + 32)) & 1ull);
+          uint32_t best = 0u;
+          int bs = -1;
+          if (a0) {
+            best = hk0;
+            bs = lane;
+          }
+          if (a1 && (bs < 0 || hk1 > best)) {
+            best = hk1;
+            bs = lane + 32;
+          }
+          const uint32_t km = __reduce_max_sync(0xffffffffu, bs < 0 ? 0u : best);
+          const int win = (int)__reduce_min_sync(0xffffffffu, (bs >= 0 && best == km) ? (uint32_t)bs : 0xffffffffu);
+          pick[np++] = win;
+          evm |= 1ull << win;
+        }
+        for (int c = 0; c < np; c += 4) {
+          int e4[4], s4[4];
+          float v4[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) e4[j] = cand_e[wp][min(c + j, n - 1)];
-        exact_logits4(xr, wr, bias, H, lane, e4, v4);
+          for (int j = 0; j < 4; ++j) {
+            s4[j] = pick[min(c + j, np - 1)];
+            e4[j] = cand_e[wp][s4[j]];
+          }
+          exact_logits4(xr, wr, bias, H, lane, e4, v4);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (lane == j && c + j < n) cand_v[wp][c + j] = v4[j];
+          for (int j = 0; j < 4; ++j)
+            if (lane == j && c + j < np) cand_v[wp][s4[j]] = v4[j];
+        }
+        nev += np;
+        __syncwarp();
+        if (nev >= n) break;
+        // the k-th largest computed logit, counted with multiplicity (nev >= k)
+        const bool c0 = s0 && ((evm >> lane) & 1ull), c1 = s1 && ((evm >> (lane + 32)) & 1ull);
+        const uint32_t vk0 = c0 ? logit_key(cand_v[wp][lane]) : 0u, vk1 = c1 ? logit_key(cand_v[wp][lane + 32]) : 0u;
+        uint32_t cur = 0xffffffffu, kth = 0u;
+        int need = k;
+        for (int r = 0; r < k; ++r) {
+          uint32_t best = 0u;
+          if (c0 && vk0 < cur && vk0 > best) best = vk0;
+          if (c1 && vk1 < cur && vk1 > best) best = vk1;
+          const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+          const uint32_t cnt = __reduce_add_sync(0xffffffffu, (c0 && vk0 == m ? 1u : 0u) + (c1 && vk1 == m ? 1u : 0u));
+          kth = m;
+          if ((int)cnt >= need) break;
+          need -= (int)cnt;
+          cur = m;
+        }
+        // the largest upper bound among the candidates not computed
+        uint32_t hu = 0u;
+        if (s0 && !c0) hu = hk0;
+        if (s1 && !c1 && hk1 > hu) hu = hk1;
+        hu = __reduce_max_sync(0xffffffffu, hu);
+        if (hu < kth) break;
+        batch = 4;
       }
-      __syncwarp();
-      // top-k over the candidates (slot lane, then lane + 32: ascending expert)
-      const bool h0 = lane < n, h1 = lane + 32 < n;
+      // top-k over the computed candidates (slot lane, then lane + 32: ascending expert)
+      const bool h0 = s0 && ((evm >> lane) & 1ull), h1 = s1 && ((evm >> (lane + 32)) & 1ull);
       const int e0 = h0 ? cand_e[wp][lane] : 0, e1 = h1 ? cand_e[wp][lane + 32] : 0;
       const float v0 = h0 ? cand_v[wp][lane] : 0.0f, v1 = h1 ? cand_v[wp][lane + 32] : 0.0f;
       bool tk0 = false, tk1 = false;
@@ -510,9 +576,10 @@ __global__ void __launch_bounds__(256) pf_select_kernel(const uint16_t* __restri
       }
       __syncwarp();
       row_topk(row, E, k, lane, chosen, cv);
+      nev = E;
     }
     write_routing(t, k, lane, chosen, cv, idx, wout);
-    if (lane == 0) nexact[wp] = n;
+    if (lane == 0) nexact[wp] = nev;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
