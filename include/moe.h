@@ -48,7 +48,7 @@ typedef enum moe_status {
   MOE_ERR_CUDA = 3,        /* a CUDA call failed (text in moe_last_error) */
   MOE_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (latched; see moe_layer_forward) */
   MOE_ERR_STATE = 5,       /* call not valid in the plan's current state */
-  MOE_ERR_UNSUPPORTED = 6  /* well-formed request outside what this build implements */
+  MOE_ERR_UNSUPPORTED = 6  /* well-formed request outside what the library implements */
 } moe_status;
 
 typedef enum moe_scale_dtype { MOE_SCALE_F32 = 0, MOE_SCALE_BF16 = 1, MOE_SCALE_F16 = 2 } moe_scale_dtype;

@@ -479,7 +479,7 @@ extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out)
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, desc->device);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, desc->device);
   if (major != 10 || minor != 3)
-    return fail(nullptr, MOE_ERR_UNSUPPORTED, "this build targets sm_103a (GB300) only");
+    return fail(nullptr, MOE_ERR_UNSUPPORTED, "the library targets sm_103a (GB300) only");
 
   Plan* p = new (std::nothrow) Plan();
   if (!p) return fail(nullptr, MOE_ERR_OOM, "host allocation failed");
