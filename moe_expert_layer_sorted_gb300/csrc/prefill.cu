@@ -3,29 +3,37 @@
 // E experts, the layer output the routing-weighted sum of the experts'
 // SwiGLU FFNs), as a chain of launches on the caller's stream:
 //
-//   1. pf_router_kernel   fp32 router logits in the library's fixed summation
-//                         order (lane j of a warp owns elements 256m + 8j + r;
-//                         xor-butterfly; bias last), tiled 32 tokens x 16
-//                         experts per CTA (8 x 8 per warp), operands staged
-//                         as bf16 with cp.async in a four-block ring.
-//   2. pf_topk_kernel     per token: k largest logits (ties -> lower expert
-//                         index), softmax renormalised over the k.
-//   3. pf_bucket_count / pf_bucket_scan / pf_bucket_place
+//   1. routing, the top-k of the router logits in the library's fixed
+//      summation order (lane j of a warp owns elements 256m + 8j + r;
+//      xor-butterfly; bias last), ties -> lower expert index, softmax
+//      renormalised over the k:
+//      - a bf16 cuBLAS GEMM for approximate logits, then pf_select_kernel (one
+//        warp per token): a rigorous bound on each approximate logit's
+//        distance to the fixed-order one, the fixed-order logits of the
+//        experts that can still reach the top-k only, the top-k over those
+//        (see "bounded router" below);
+//      - or, when the caller asks for the logits, pf_router_kernel (every
+//        logit in the fixed order, tiled 32 tokens x 16 experts per CTA,
+//        8 x 8 per warp, operands staged as bf16 with cp.async in a
+//        four-block ring) and pf_topk_kernel.
+//   2. pf_bucket_count / pf_bucket_scan / pf_bucket_place
 //                         grouping by expert: a stable counting sort of the
 //                         slots (per-block expert histograms, one prefix over
 //                         (expert, block), placement in slot order) giving
 //                         per-expert counts, offsets and the (expert, token)
 //                         order perm / inv.
-//   4. pf_gather_kernel   the layer input's rows copied into grouped
-//                         (expert, token) order.
-//   5. pf_gemm_kernel<gate/up>  for every routed (expert, 128 of its tokens,
+//   3. pf_gather_kernel   the layer input's rows copied into grouped
+//                         (expert, token) order, columns in the GEMMs' stage
+//                         K order.
+//   4. pf_gemm_kernel<gate/up>  for every routed (expert, 128 of its tokens,
 //                         128 rows of I): gate and up projections on tcgen05
 //                         tensor cores (M = 128 tokens, N = 128 gate + 128 up
 //                         rows) with fp32 accumulators in TMEM; the epilogue
 //                         writes h = silu(g) * u (bf16) per (token, expert) slot.
-//   6. pf_gemm_kernel<down>  o = Wd h per (expert, 128 tokens, 256 rows of H),
+//   5. pf_gemm_kernel<down>  o = Wd h per (expert, 128 tokens, 256 rows of H),
 //                         times the slot's routing weight, bf16 per slot.
-//   7. pf_combine_kernel  y[t] = sum over j ascending of the slot outputs, bf16.
+//   6. pf_combine_kernel  y[t] = sum over j ascending of the slot outputs, bf16.
+//   7. pf_stats_kernel    the forward's accounting.
 //
 // GEMM kernel layout (one CTA of 23 warps per SM, persistent over work units,
 // consecutive units of an expert sharing its token tile):
