@@ -40,9 +40,12 @@ def _check(plan, wl, wr, bias, x):
 
 
 LONGH = W.Workload("prefill-long-h", 1, 16, 4352, 256, 2, (24,), 3, 128, W.SC_BF16, "plain")
+K8 = W.Workload("prefill-k8", 1, 96, 512, 256, 8, (200,), 4, 64, W.SC_BF16, "zipf", 1.0)   # k = 8: the first
+K1 = W.Workload("prefill-k1", 1, 96, 512, 256, 1, (200,), 4, 64, W.SC_BF16, "zipf", 1.0)   # round is k; k = 1
 
 
-@pytest.mark.parametrize("wl,T", [(MID, 9), (MID, 300), (MID3, 700), (MID2, 600), (WIDEP, 40), (LONGH, 24)])
+@pytest.mark.parametrize("wl,T", [(MID, 9), (MID, 300), (MID3, 700), (MID2, 600), (WIDEP, 40), (LONGH, 24),
+                                  (K8, 200), (K1, 200)])
 def test_bounded_router_matches_the_fixed_order(wl, T):
     from moe_expert_layer_sorted_gb300 import harness
     plan, info = harness.build_plan(wl, max_tokens=T)
