@@ -28,8 +28,12 @@
  *  - A plan is used by one host thread at a time.  Calls that enqueue work
  *    are ordered on the stream given; a forward on a different stream than
  *    the previous one first waits for the previous one (the plan's scratch
- *    buffers are reused).  A call made while another call on the same plan
- *    is running on another thread returns MOE_ERR_STATE.
+ *    buffers are reused).  Forwards enqueued while their stream is being
+ *    captured into a CUDA graph take no part in that ordering (the graph's
+ *    own edges order its nodes): the caller orders a graph's launches
+ *    against the plan's other work, as for any graph.  A call made while
+ *    another call on the same plan is running on another thread returns
+ *    MOE_ERR_STATE.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

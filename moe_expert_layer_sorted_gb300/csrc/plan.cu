@@ -460,6 +460,30 @@ void release(Plan* p) {
   delete p;
 }
 
+// Cross-stream ordering of a plan's forwards (they share its scratch): a
+// forward on another stream than the previous one waits for it.  While the
+// stream is being captured into a graph nothing is waited on or recorded --
+// the graph's edges order its nodes, and an event recorded inside a capture
+// could not be waited on by a later forward outside it.
+cudaError_t order_before(Plan* p, cudaStream_t s, bool& capturing) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &st);
+  if (e != cudaSuccess) return e;
+  capturing = st != cudaStreamCaptureStatusNone;
+  if (!capturing && p->have_last && p->last_stream != s) return cudaStreamWaitEvent(s, p->ev_done, 0);
+  return cudaSuccess;
+}
+
+cudaError_t order_after(Plan* p, cudaStream_t s, bool capturing) {
+  if (capturing) return cudaSuccess;
+  const cudaError_t e = cudaEventRecord(p->ev_done, s);
+  if (e == cudaSuccess) {
+    p->last_stream = s;
+    p->have_last = true;
+  }
+  return e;
+}
+
 }  // namespace
 
 extern "C" moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out) {
@@ -880,14 +904,13 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
   }
   if (take_overflow(p)) return fail(p, MOE_ERR_STATE, kOverflowMsg);
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->have_last && p->last_stream != s) CK(p, cudaStreamWaitEvent(s, p->ev_done, 0));
+  bool capturing = false;
+  CK(p, order_before(p, s, capturing));
   cudaError_t e;
   if (T <= kDecodeMaxTokens) e = decode_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
   else e = prefill_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
   if (e != cudaSuccess) return cuda_fail(p, e, "forward launch");
-  CK(p, cudaEventRecord(p->ev_done, s));
-  p->last_stream = s;
-  p->have_last = true;
+  CK(p, order_after(p, s, capturing));
   return MOE_OK;
 }
 
@@ -913,7 +936,8 @@ extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void*
   if (*p->err_host) return fail(p, MOE_ERR_STATE, "a latched device error is pending: call moe_layer_forward");
   if (take_overflow(p)) return fail(p, MOE_ERR_STATE, kOverflowMsg);
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->have_last && p->last_stream != s) CK(p, cudaStreamWaitEvent(s, p->ev_done, 0));
+  bool capturing = false;
+  CK(p, order_before(p, s, capturing));
   const int64_t chunk = std::min<int64_t>(8192, d.max_tokens), H = d.hidden;
   // Staging pays back only over several chunks (it moves each host expert
   // over the link once instead of once per chunk): with one chunk every
@@ -930,9 +954,7 @@ extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void*
                         stage ? p->pf_blob : nullptr);
     if (e != cudaSuccess) return cuda_fail(p, e, "prefill chunk");
   }
-  CK(p, cudaEventRecord(p->ev_done, s));
-  p->last_stream = s;
-  p->have_last = true;
+  CK(p, order_after(p, s, capturing));
   return MOE_OK;
 }
 

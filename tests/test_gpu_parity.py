@@ -115,6 +115,31 @@ def test_host_buffer_forward_matches_device_forward(tiny):
     assert torch.equal(yh, y_dev.view(torch.int16).cpu())
 
 
+def test_captured_forward_then_forward_on_another_stream(tiny):
+    """A forward captured into a CUDA graph takes no part in the plan's
+    cross-stream ordering; replays and ordinary forwards on other streams
+    afterwards give the same bits."""
+    torch = _torch()
+    wl, plan, _, _ = tiny
+    x = torch.from_numpy(W.tokens(wl, 21, 0, 8).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y_ref = torch.empty_like(x)
+    plan.forward(0, x, y_ref)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    y_g = torch.empty_like(x)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=a):
+        plan.forward(0, x, y_g, stream=a)
+    g.replay()
+    torch.cuda.synchronize()
+    y_b = torch.empty_like(x)
+    with torch.cuda.stream(b):
+        plan.forward(0, x, y_b, stream=b)
+    torch.cuda.synchronize()
+    assert torch.equal(y_g.view(torch.int16), y_ref.view(torch.int16))
+    assert torch.equal(y_b.view(torch.int16), y_ref.view(torch.int16))
+
+
 def test_placement_changes_no_output_bit():
     """Same layer placed all-HBM, all-host and mixed: identical y bits."""
     torch = _torch()
