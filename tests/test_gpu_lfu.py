@@ -119,7 +119,9 @@ def plan_expert_bytes(wl):
 # rounds per thread; counts halved every 16 steps; eight tokens per step so
 # that the run touches more experts than the cache holds and evicts.  The
 # expert matrices keep the cached workload's shape (H=2048, I=512, int2 G64
-# fp16 scales): the cache rules do not depend on it, the bytes do.
+# fp16 scales): the cache rules do not depend on it, the bytes do.  At the
+# last step three layers' outputs (experts read from cache slots and in place
+# from host memory) are checked against the oracle as well.
 WL_FULL = W.Workload("lfu-full", 48, 512, 2048, 512, 8, (8,), 2, 64, W.SC_F16, "zipf", 1.2,
                      cache_frac=0.7, steps=320, drift=0.01)
 AGING = 16
@@ -147,9 +149,15 @@ def test_lfu_full_size_with_aging_matches_cache_simulator():
     misses = np.zeros((S, L), np.int64)
     adm = evi = 0  # the step ends' admissions and evictions, summed over the per-layer reads
     plan.stats(-1, reset=True)
+    check = (0, 29, L - 1)  # layers whose outputs at the last step go to the oracle
+    y_last = {l: torch.empty(T, wl.hidden, dtype=torch.bfloat16, device="cuda") for l in check}
+    bias_last = None
     for s in range(S):
+        if s == S - 1:
+            bias_last = biases.copy()
         for l in range(L):
-            plan.forward(l, xs[s, l], y, dbg=dict(topk_idx=idx_all[s, l]))
+            out = y_last[l] if (s == S - 1 and l in check) else y
+            plan.forward(l, xs[s, l], out, dbg=dict(topk_idx=idx_all[s, l]))
         for l in range(L):
             st = plan.stats(l, reset=True)
             hits[s, l], misses[s, l] = st["hits"], st["misses"]
@@ -171,6 +179,25 @@ def test_lfu_full_size_with_aging_matches_cache_simulator():
     adm += tot["admissions"]
     evi += tot["evictions"]
     slot_of = np.concatenate([plan.residence(l) for l in range(L)])
+    # outputs of the last step's checked layers (experts read from cache slots
+    # and in place from host memory) against the oracle, with that step's biases
+    for l in check:
+        x_bits = xs[S - 1, l].view(torch.int16).cpu().numpy().view(np.uint16)
+        wr = info["routers"][l][0]
+        used = np.unique(idx[S - 1, l])
+        experts = [None] * E
+        for e in used:
+            q = [oracle.quantize(W.expert_master(wl, l, int(e), m), wl.bits, wl.group, wl.scale_dtype)
+                 for m in range(3)]
+            experts[int(e)] = oracle.QuantExpert([c for c, _ in q], [sc for _, sc in q])
+        lg = oracle.router_logits(x_bits, wr, bias_last[l])
+        o_idx, _ = oracle.topk(lg, k)
+        assert np.array_equal(idx[S - 1, l], o_idx), l
+        ref = oracle.layer_forward_tokens(experts, wl.hidden, wl.inter, k, wl.bits, wl.group, wl.scale_dtype,
+                                          x_bits, wr, bias_last[l], np.arange(T))
+        yg = oracle.bf16_to_f32(y_last[l].view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+        err = float((np.abs(yg - ref).max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-30)).max())
+        assert err <= 1e-2, (l, err)
     plan.close()
     assert sim["evictions"] > 1000, sim["evictions"]  # the cache filled and kept turning over
     np.testing.assert_array_equal(hits, sim["hits"])
