@@ -119,3 +119,27 @@ def test_bounded_router_full_size():
     print(f"fixed-order logits per token: {per_token:.2f} of {wl.experts}")
     assert wl.top_k <= per_token < 0.1 * wl.experts
     plan.close()
+
+
+def test_prefill_forward_in_a_cuda_graph():
+    """The prefill forward (its cuBLAS GEMM included, on the plan's own
+    workspace) captured into a CUDA graph and replayed gives the eager
+    forward's bits."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    wl, T = MID3, 700
+    plan, _ = harness.build_plan(wl, max_tokens=T)
+    x = torch.from_numpy(W.tokens(wl, 99, 0, T).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y_ref, y_g = torch.empty_like(x), torch.empty_like(x)
+    plan.forward(0, x, y_ref)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.forward(0, x, y_g, stream=s)
+    for _ in range(2):
+        y_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y_g.view(torch.int16), y_ref.view(torch.int16))
+    plan.close()
