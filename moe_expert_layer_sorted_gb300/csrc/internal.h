@@ -104,6 +104,7 @@ struct Plan {
   // prefill routing: cuBLAS handle with a workspace of its own (no allocation in a forward)
   cublasHandle_t blas = nullptr;
   void* blas_ws = nullptr;
+  int blas_status = 0;  // a failed cuBLAS call of the last prefill forward (reported, then cleared)
   static constexpr size_t kBlasWorkspace = size_t(32) << 20;
 
   // forward scratch (device)

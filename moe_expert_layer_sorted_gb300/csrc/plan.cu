@@ -34,6 +34,18 @@ moe_status cuda_fail(Plan* p, cudaError_t e, const char* what) {
   return fail(p, MOE_ERR_CUDA, m);
 }
 
+// A forward's launch failure; a failed cuBLAS call (the prefill router's
+// logits GEMM) is reported with its own status.
+moe_status forward_fail(Plan* p, cudaError_t e, const char* what) {
+  if (p && p->blas_status) {
+    const int bs = p->blas_status;
+    p->blas_status = 0;
+    return fail(p, MOE_ERR_CUDA, std::string(what) + ": the router logits GEMM (cuBLAS) failed with status " +
+                                     std::to_string(bs));
+  }
+  return cuda_fail(p, e, what);
+}
+
 #define CK(p, call)                                          \
   do {                                                       \
     cudaError_t e_ = (call);                                 \
@@ -909,7 +921,7 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
   cudaError_t e;
   if (T <= kDecodeMaxTokens) e = decode_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
   else e = prefill_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
-  if (e != cudaSuccess) return cuda_fail(p, e, "forward launch");
+  if (e != cudaSuccess) return forward_fail(p, e, "forward launch");
   CK(p, order_after(p, s, capturing));
   return MOE_OK;
 }
@@ -952,7 +964,7 @@ extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void*
     e = prefill_forward(*p, layer, static_cast<const uint16_t*>(x) + off * H, tc,
                         static_cast<uint16_t*>(y) + off * H, s, nullptr, /*lfu=*/false,
                         stage ? p->pf_blob : nullptr);
-    if (e != cudaSuccess) return cuda_fail(p, e, "prefill chunk");
+    if (e != cudaSuccess) return forward_fail(p, e, "prefill chunk");
   }
   CK(p, order_after(p, s, capturing));
   return MOE_OK;

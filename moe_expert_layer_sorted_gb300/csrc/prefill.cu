@@ -1443,11 +1443,14 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     pf_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(p.logits, T, E, k, p.topk_idx, p.topk_w);
   } else {  // bounded tensor-core logits, then the fixed order for the candidates only
     const float one = 1.0f, zero = 0.0f;
-    if (cublasSetStream(p.blas, s) != CUBLAS_STATUS_SUCCESS ||
-        cublasGemmEx(p.blas, CUBLAS_OP_T, CUBLAS_OP_N, E, T, H, &one, p.wr[layer], CUDA_R_16BF, H, x,
-                     CUDA_R_16BF, H, &zero, p.logits, CUDA_R_32F, E, CUBLAS_COMPUTE_32F,
-                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return cudaErrorLaunchFailure;
+    cublasStatus_t bs = cublasSetStream(p.blas, s);
+    if (bs == CUBLAS_STATUS_SUCCESS)
+      bs = cublasGemmEx(p.blas, CUBLAS_OP_T, CUBLAS_OP_N, E, T, H, &one, p.wr[layer], CUDA_R_16BF, H, x,
+                        CUDA_R_16BF, H, &zero, p.logits, CUDA_R_32F, E, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    if (bs != CUBLAS_STATUS_SUCCESS) {  // the caller reports the cuBLAS status
+      p.blas_status = (int)bs;
+      return cudaErrorUnknown;
+    }
     if (E <= 16 * 32)
       pf_select_kernel<16><<<(T + 7) / 8, 256, 0, s>>>(x, T, H, p.wr[layer], p.bias[layer],
                                                        p.wnorm_all + (int64_t)layer * E, E, k, p.logits,
