@@ -938,11 +938,18 @@ __device__ __forceinline__ void dequant_tiles(const GemmArgs& a, const DqRings& 
           uint32_t w[4];
           chunk_words<B>(citem, lane, q, w);
           float sc[4];  // rows g, g+8 of the stage's column halves 0 and 1
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint8_t* rec = sitem + ((q * 64 + 32 * h) >> lg_g) * (16 * ssz);
-            sc[2 * h] = scale_of<SDT>(rec, g);
-            sc[2 * h + 1] = scale_of<SDT>(rec, g + 8);
+          {
+            const uint8_t* rec = sitem + ((q * 64) >> lg_g) * (16 * ssz);
+            sc[0] = scale_of<SDT>(rec, g);
+            sc[1] = scale_of<SDT>(rec, g + 8);
+            if (a.G >= 64) {  // both halves in one scale group: no second pair of loads
+              sc[2] = sc[0];
+              sc[3] = sc[1];
+            } else {
+              const uint8_t* rec1 = sitem + ((q * 64 + 32) >> lg_g) * (16 * ssz);
+              sc[2] = scale_of<SDT>(rec1, g);
+              sc[3] = scale_of<SDT>(rec1, g + 8);
+            }
           }
           uint32_t out[16];  // pair i: MMA step i/4 of the stage, fragment register i%4
           if constexpr (SDT == MOE_SCALE_BF16) {  // (128 + u) - zb is exact in bf16; one rounding for the product
