@@ -119,6 +119,16 @@ class L2Flush:
         self.r.sum()
 
 
+def gpu_hold(seconds: float = 0.05):
+    """Keep the GPU busy for about `seconds` (a sleep kernel on the current
+    stream) while the host enqueues the timed steps behind it: the steps then
+    run back to back on the GPU, and a pause of the host thread (a driver
+    call of the clock sampler, the interpreter) does not show up as idle GPU
+    time inside a step's events.  Placed before the first timed event."""
+    import torch
+    torch.cuda._sleep(int(seconds * 2.1e9))
+
+
 class ClockSampler:
     """SM clocks and clock-event (throttle) reasons sampled during the timed
     region.  The timed region of a decode step is a few milliseconds, shorter
@@ -417,6 +427,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     with torch.cuda.stream(stream):
+        gpu_hold()
         for i in range(args.steps):
             flush()
             a = torch.cuda.Event(enable_timing=True)
@@ -653,6 +664,7 @@ def run_stack(args):
         clocks.start()
         ev = []
         with torch.cuda.stream(stream):
+            gpu_hold()
             for st in range(args.warmup, nsteps):
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
@@ -762,12 +774,14 @@ def run_cached(args):
     b = torch.cuda.Event(enable_timing=True)
     st_half = None
     with torch.cuda.stream(stream):
+        gpu_hold()
         a.record(stream)
         for st in range(S):
             if st == half:  # counters of the first half: read between the two timed halves
                 m.record(stream)
                 stream.synchronize()
                 st_half = plan.stats(-1)
+                gpu_hold()
                 m2.record(stream)
             stage(st)
             g.replay()
@@ -832,6 +846,7 @@ def prefill_measure(args, steps: int, warmup: int, cpu: bool = True) -> dict:
     clocks.start()
     ev = []
     with torch.cuda.stream(stream):
+        gpu_hold()
         for i in range(steps):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
