@@ -1154,41 +1154,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
   } else if (warp == kTokWarp) {
     // ------------------------------------------------------------ token rows
     // Per stage: the unit's 128 token rows x 64 columns by one tensor copy.
+    // Every lane waits on the barriers (a warp-wide wait wakes sooner than
+    // one lane's while the other lanes sit at a warp barrier); lane 0 issues.
     RingPos tp;
     int ntfill = 0;
-    if (lane == 0) {
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-        int e, rt, n0, nrows;
-        decode_unit(u, e, rt, n0, nrows);
-        for (int s = 0; s < S; ++s) {
-          const int slot = tp.slot;
-          mbar_wait<false>(smem_addr(&tokEmpty[slot]), tp.phase ^ 1u, a.err);
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      int e, rt, n0, nrows;
+      decode_unit(u, e, rt, n0, nrows);
+      for (int s = 0; s < S; ++s) {
+        const int slot = tp.slot;
+        mbar_wait<false>(smem_addr(&tokEmpty[slot]), tp.phase ^ 1u, a.err);
+        if (lane == 0) {
           const uint32_t bar = smem_addr(&tokFull[slot]);
           mbar_arrive_expect_tx(bar, kTokBytes);
           tma_load_2d(smem_addr(tokr + (size_t)slot * kTokBytes), &tok_map, s * kStageK, n0, bar);
-          tp.next(a.nt);
-          ++ntfill;
         }
+        __syncwarp();
+        tp.next(a.nt);
+        ++ntfill;
       }
-      for (int q = 0; q < a.nt && q < ntfill; ++q) mbar_drain(smem_addr(&tokFull[q]), tp.last_parity(q));
     }
+    for (int q = 0; q < a.nt && q < ntfill; ++q) mbar_drain(smem_addr(&tokFull[q]), tp.last_parity(q));
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kTileM, kTileN);
-      RingPos tp, wp;
-      int ui = 0;
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
-        const int buf = ui & 1;
-        mbar_wait<false>(smem_addr(&tempty[buf]), ((uint32_t)(ui >> 1) & 1u) ^ 1u, a.err);  // accumulator free
+    // The whole warp waits; lane 0 issues the MMAs and the commits.
+    const uint32_t idesc = idesc_bf16(kTileM, kTileN);
+    RingPos tp, wp;
+    int ui = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
+      const int buf = ui & 1;
+      mbar_wait<false>(smem_addr(&tempty[buf]), ((uint32_t)(ui >> 1) & 1u) ^ 1u, a.err);  // accumulator free
+      tc_fence_after();
+      const uint32_t dacc = tmem + (uint32_t)(buf * 256);
+      for (int s = 0; s < S; ++s) {
+        const int ts = tp.slot, wsl = wp.slot;
+        mbar_wait<false>(smem_addr(&tokFull[ts]), tp.phase, a.err);
+        mbar_wait<false>(smem_addr(&wFull[wsl]), wp.phase, a.err);
         tc_fence_after();
-        const uint32_t dacc = tmem + (uint32_t)(buf * 256);
-        for (int s = 0; s < S; ++s) {
-          const int ts = tp.slot, wsl = wp.slot;
-          mbar_wait<false>(smem_addr(&tokFull[ts]), tp.phase, a.err);
-          mbar_wait<false>(smem_addr(&wFull[wsl]), wp.phase, a.err);
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t at = smem_addr(tokr + (size_t)ts * kTokBytes);
           const uint32_t bt = smem_addr(wr + (size_t)wsl * kWBytes);
 #pragma unroll
@@ -1196,14 +1200,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
             umma_bf16(dacc, smem_desc_sw128(at + j * 32), smem_desc_sw128(bt + j * 32), idesc, (s | j) ? 1u : 0u);
           umma_commit(smem_addr(&tokEmpty[ts]));  // both stages are free once these MMAs are done
           umma_commit(smem_addr(&wEmpty[wsl]));
-          tp.next(a.nt);
-          wp.next(a.nw);
         }
-        umma_commit(smem_addr(&tfull[buf]));
+        __syncwarp();
+        tp.next(a.nt);
+        wp.next(a.nw);
       }
-      // the last MMAs have completed before TMEM is released
-      for (int j = max(0, ui - 2); j < ui; ++j) mbar_drain(smem_addr(&tfull[j & 1]), (uint32_t)(j >> 1) & 1u);
+      if (lane == 0) umma_commit(smem_addr(&tfull[buf]));
+      __syncwarp();
     }
+    // the last MMAs have completed before TMEM is released
+    for (int j = max(0, ui - 2); j < ui; ++j) mbar_drain(smem_addr(&tfull[j & 1]), (uint32_t)(j >> 1) & 1u);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 16-19)
