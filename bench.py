@@ -542,6 +542,10 @@ def run_ours(args):
         # the prefill layer (tensor-core path) in the same run, as an extra key
         pre = prefill_measure(args, steps=max(5, min(args.steps, 20)), warmup=3, cpu=not args.no_cpu)
         line["prefill"] = pre
+    if rank == 0 and not args.no_stacks:
+        # the 40-layer stack and the cached 48-layer decode in the same run, as extra keys
+        line["stack40"] = stack_measure(args)
+        line["cached"] = cached_measure(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -608,8 +612,13 @@ def _common_line(args, metric, value, unit, ms, config, extra):
 
 
 def run_stack(args):
+    print(json.dumps(stack_measure(args)), flush=True)
+
+
+def stack_measure(args) -> dict:
     """40-layer stack of the decode layer (config "stack40"): each step feeds
-    T fresh tokens through all 40 layers, layer l+1 taking bf16(y_l + noise)."""
+    T fresh tokens through all 40 layers, layer l+1 taking bf16(y_l + noise).
+    Returns the measurement as a dict (the keys of a bench line)."""
     import torch
     import synth
     from moe_expert_layer_sorted_gb300 import harness, probe_bandwidth
@@ -699,14 +708,19 @@ def run_stack(args):
                       "frac_max_form": per_T[T_head]["roofline_frac_max_form"],
                       "peak_note": f"sum form: HBM {hbm_peak:.0f} GB/s ({peak_kind}) + host link {link_gbs:.1f} GB/s"},
          "gpu_launches": launches, "clocks": per_T[T_head]["clocks"]})
-    print(json.dumps(line), flush=True)
     plan.close()
+    return line
 
 
 def run_cached(args):
+    print(json.dumps(cached_measure(args)), flush=True)
+
+
+def cached_measure(args) -> dict:
     """Cached decode (config "cached"): 48 layers, all experts in pinned host
     memory, LFU cache of 70% of them in HBM, one token per step, router bias
-    drifting per step; every step ends with the cache's admission pass."""
+    drifting per step; every step ends with the cache's admission pass.
+    Returns the measurement as a dict (the keys of a bench line)."""
     import torch
     import synth
     from moe_expert_layer_sorted_gb300 import harness, probe_bandwidth
@@ -810,8 +824,8 @@ def run_cached(args):
          "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
                   "gpu": _numa_node(0)},
          "setup_s": build_s, "gpu_launches": (3 * L + 2) * S, "clocks": ck})  # per layer: router, expert kernel, next input; step end: 2
-    print(json.dumps(line), flush=True)
     plan.close()
+    return line
 
 
 def prefill_measure(args, steps: int, warmup: int, cpu: bool = True) -> dict:
@@ -1231,6 +1245,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode: leave out the prefill key")
+    ap.add_argument("--no-stacks", action="store_true", help="decode: leave out the stack40 and cached keys")
     ap.add_argument("--workload", default="decode", choices=["decode", "stack40", "cached", "prefill",
                                                               "cpu-vs-uva", "prefetch-bound",
                                                               "prefill-staging", "prefill-chunked",
