@@ -85,7 +85,6 @@ struct Plan {
   uint8_t* host_arena = nullptr;      // pinned, mapped
   uint8_t* host_arena_dev = nullptr;  // its device alias
   int64_t host_cap = 0, host_used = 0;
-  bool host_mmap = false;  // host arena = NUMA-bound mapping registered with CUDA (else cudaHostAlloc)
   int numa_node = -1;      // the GPU's NUMA node the host arena was bound to (-1: none)
 
   // residence (device tables [L*E]) and host mirrors
