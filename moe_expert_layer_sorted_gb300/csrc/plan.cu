@@ -118,22 +118,28 @@ int gpu_numa_node(int device) {
 
 // Pinned, device-mapped host memory of `bytes` from the driver's pinned
 // allocator (cudaHostAlloc).  When node >= 0 the calling thread prefers that
-// NUMA node for the call (set_mempolicy MPOL_PREFERRED, default policy restored
-// after), so the pages come from the GPU's node where the system places them
+// NUMA node for the call (set_mempolicy MPOL_PREFERRED, the thread's own policy
+// restored after), so the pages come from the GPU's node where the system places them
 // by the caller's policy.  The driver's allocator is used rather than
 // page-locking an anonymous mapping: on a host whose memory earlier large
 // pinned arenas had churned, the GPU read such a registered mapping several
 // times slower (a decode step of the decode layer 0.55-0.72 ms against 0.26 ms
 // from cudaHostAlloc; on a fresh host both 0.20 ms).
 void* pinned_alloc(size_t bytes, int node) {
+  // the calling thread's own policy, restored after the call
+  int old_mode = 0;
+  unsigned long old_mask[16] = {0};  // up to 1024 nodes
   bool preferred = false;
-  if (node >= 0 && node < 64) {
+  if (node >= 0 && node < 64 && syscall(SYS_get_mempolicy, &old_mode, old_mask, 1024ul, nullptr, 0ul) == 0) {
     unsigned long mask = 1ul << node;
     preferred = syscall(SYS_set_mempolicy, 1 /* MPOL_PREFERRED */, &mask, 64ul) == 0;
   }
   void* h = nullptr;
   const cudaError_t e = cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (preferred) syscall(SYS_set_mempolicy, 0 /* MPOL_DEFAULT */, nullptr, 0ul);
+  if (preferred) {
+    const bool dflt = (old_mode & 0xff) == 0;  // MPOL_DEFAULT (mode flags in the high bits)
+    syscall(SYS_set_mempolicy, old_mode, dflt ? nullptr : old_mask, dflt ? 0ul : 1024ul);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
