@@ -145,9 +145,10 @@ typedef struct moe_cache_stats_t {
  * dies under load is the failure "125B sparse model on one 32 GB consumer
  * card" describes in section "A compute buffer is what limits capacity";
  * allocates the HBM expert arena (STATIC) or slot arena (LFU), the pinned host
- * arena (every expert not in HBM; all experts under LFU) on the GPU's NUMA
- * node where the system reports one ("763B MoE in two 96 GB cards", section
- * "PCIe topology"), and all scratch.  *out is set on success.  Test hook:
+ * arena (every expert not in HBM; all experts under LFU; from the driver's
+ * pinned allocator with the GPU's NUMA node preferred where the system reports
+ * one, "763B MoE in two 96 GB cards", section "PCIe topology"), and all
+ * scratch.  *out is set on success.  Test hook:
  * the environment variable MOE_FAULT containing "hbm_alloc" or
  * "pinned_alloc" makes that allocation fail (MOE_ERR_OOM, all released). */
 moe_status moe_plan_create(const moe_plan_desc* desc, moe_plan** out);
