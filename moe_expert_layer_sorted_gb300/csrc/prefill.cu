@@ -840,6 +840,14 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[1
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// one 32-byte global store (p 32-byte aligned): a whole sector per thread
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t w4,
+                                             uint32_t w5, uint32_t w6, uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2), "r"(w3),
+               "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
 // 2-D tiled tensor copy (box of the map) global -> shared, completing on bar
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
@@ -1262,11 +1270,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
 #pragma unroll
           for (int c = 0; c < 16; c += 2)
             op[c >> 1] = pack_bf16x2(wgt * __uint_as_float(v[c]), wgt * __uint_as_float(v[c + 1]));
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + rt * 256 + c0);
-            dst[0] = make_uint4(op[0], op[1], op[2], op[3]);
-            dst[1] = make_uint4(op[4], op[5], op[6], op[7]);
-          }
+          if (live) st_global_v8(orow + rt * 256 + c0, op[0], op[1], op[2], op[3], op[4], op[5], op[6], op[7]);
         }
       }
       tc_fence_before();
