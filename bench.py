@@ -651,9 +651,8 @@ def stack_measure(args) -> dict:
         def body(st):
             xs[0].view(torch.int16).copy_(x0[st])
             for l in range(L):
-                plan.forward(l, xs[l], ys[l], stream=torch.cuda.current_stream())
-                synth.residual_bf16_device(ys[l].data_ptr(), noise[st, l].data_ptr(), T * H, xs[l + 1].data_ptr(),
-                                           torch.cuda.current_stream().cuda_stream)
+                # layer output and the next layer's input bf16(y_l + noise) in one forward
+                plan.forward_residual(l, xs[l], ys[l], noise[st, l], xs[l + 1], stream=torch.cuda.current_stream())
 
         with torch.cuda.stream(stream):
             body(0)  # per-T launch configuration before capture
@@ -692,7 +691,7 @@ def stack_measure(args) -> dict:
                          "host_GB_per_step": ob / 1e9, "weight_stream_GBps": (hb + ob) / (ms * 1e-3) / 1e9,
                          "roofline_ms": roof * 1e3, "roofline_frac": roof / (ms * 1e-3),
                          "roofline_frac_max_form": roof_max / (ms * 1e-3), "clocks": ck}
-        launches = 3 * L * args.steps  # router, expert kernel, next layer's input
+        launches = 2 * L * args.steps  # router, expert kernel (which also writes the next layer's input)
         del graphs
     T_head = str(max(wl.tokens))
     line = _common_line(
@@ -758,9 +757,7 @@ def cached_measure(args) -> dict:
         xs[0].view(torch.int16).copy_(x_stage)
         plan.update_router_biases(0, bias_stage, stream=torch.cuda.current_stream())
         for l in range(L):
-            plan.forward(l, xs[l], ys[l], stream=torch.cuda.current_stream())
-            synth.residual_bf16_device(ys[l].data_ptr(), noise_stage[l].data_ptr(), T * H, xs[l + 1].data_ptr(),
-                                       torch.cuda.current_stream().cuda_stream)
+            plan.forward_residual(l, xs[l], ys[l], noise_stage[l], xs[l + 1], stream=torch.cuda.current_stream())
         plan.step_end(stream=torch.cuda.current_stream())
 
     def stage(st):
@@ -823,7 +820,7 @@ def cached_measure(args) -> dict:
          "second_half_ms_per_step": m2.elapsed_time(b) / (S - half),
          "link": {"host_zero_copy_read_GBps": link_gbs, "hbm_read_probe_GBps": hbm_probe,
                   "gpu": _numa_node(0)},
-         "setup_s": build_s, "gpu_launches": (3 * L + 2) * S, "clocks": ck})  # per layer: router, expert kernel, next input; step end: 2
+         "setup_s": build_s, "gpu_launches": (2 * L + 2) * S, "clocks": ck})  # per layer: router, expert kernel (+ next input); step end: 2
     plan.close()
     return line
 

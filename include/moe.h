@@ -200,6 +200,17 @@ moe_status moe_place_experts(moe_plan* plan, int layer, int first, int count,
 moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x_bf16, int T, void* y_bf16,
                              void* stream, const moe_routing_out* dbg);
 
+/* The same forward with the residual-stream update fused into its combine:
+ * y as moe_layer_forward, and out[t][c] = bf16(float(y[t][c]) + residual[t][c])
+ * (round to nearest even), so that a stack of layers -- consecutive MoE layers
+ * of the pages' models, each fed the previous layer's output plus the residual
+ * stream -- gets the next layer's input without a launch of its own.
+ * residual [T][H] fp32 device, out [T][H] bf16 device, both 16-byte aligned;
+ * out must not overlap x, y or residual, nor residual y (MOE_ERR_INVALID).
+ * Otherwise as moe_layer_forward (dbg is NULL here). */
+moe_status moe_layer_forward_residual(moe_plan* plan, int layer, const void* x_bf16, int T, void* y_bf16,
+                                      const float* residual, void* out_bf16, void* stream);
+
 /* Chunked prefill of a long prompt through `layer`: the prefill-aware cache of
  * "Running a 24k-expert MoE on a single 32 GB card", section 2 -- HBM slots
  * kept for the prompt's experts, and long inputs read in chunks of 8,192

@@ -26,7 +26,7 @@ POLICY_STATIC, POLICY_LFU = 0, 1
 # every symbol include/moe.h declares
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_set_router", "moe_update_router_bias",
            "moe_update_router_biases", "moe_debug_fail_next_forward",
-           "moe_place_experts", "moe_layer_forward", "moe_prefill_forward", "moe_layer_forward_host",
+           "moe_place_experts", "moe_layer_forward", "moe_layer_forward_residual", "moe_prefill_forward", "moe_layer_forward_host",
            "moe_step_end",
            "moe_cache_stats", "moe_residence_table", "moe_quantize", "moe_probe_bandwidth",
            "moe_route_noalloc", "moe_status_string", "moe_last_error"]
@@ -87,6 +87,7 @@ def lib():
         L.moe_debug_fail_next_forward.argtypes = [_P]
         L.moe_place_experts.argtypes = [_P, i32, i32, i32, _P, ctypes.POINTER(ExpertWeights)]
         L.moe_layer_forward.argtypes = [_P, i32, _P, i32, _P, _P, ctypes.POINTER(RoutingOut)]
+        L.moe_layer_forward_residual.argtypes = [_P, i32, _P, i32, _P, _P, _P, _P]
         L.moe_layer_forward_host.argtypes = [_P, i32, _P, i32, _P, _P]
         L.moe_prefill_forward.argtypes = [_P, i32, _P, ctypes.c_int64, _P, _P]
         L.moe_step_end.argtypes = [_P, _P]
@@ -209,6 +210,17 @@ class Plan:
             ro = ctypes.byref(ro)
         _check(lib().moe_layer_forward(self._h, layer, _addr(x), T, _addr(y), _stream(stream), ro),
                self._h)
+
+    def forward_residual(self, layer, x, y, residual, out, stream=None):
+        """y = the layer's output and out = bf16(y + residual) in one forward (see moe.h):
+        residual fp32 [T][H], out bf16 [T][H], on x's device."""
+        import torch
+        T = x.shape[0]
+        assert residual.dtype == torch.float32 and residual.is_contiguous() and tuple(residual.shape) == tuple(x.shape)
+        assert out.is_contiguous() and out.element_size() == 2 and tuple(out.shape) == tuple(x.shape)
+        assert residual.device == x.device and out.device == x.device
+        _check(lib().moe_layer_forward_residual(self._h, layer, _addr(x), T, _addr(y), _addr(residual), _addr(out),
+                                                _stream(stream)), self._h)
 
     def prefill_forward(self, layer, x, y, stream=None):
         """Chunked prefill of a long prompt with the plan's prefill slots (see moe.h)."""

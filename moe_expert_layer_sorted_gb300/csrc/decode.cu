@@ -228,6 +228,8 @@ struct ExpertArgs {
   unsigned long long* obuf;  // [T*k][H] tagged fp32 weighted expert outputs
   int tstride;
   uint16_t* y;
+  const float* res;  // with ysum: ysum = bf16(y + res), the residual update (nullptr: none)
+  uint16_t* ysum;
   MatOff m[3];
   int group, sdt;
   float zcorr;  // 128 + 2^(b-1)
@@ -995,6 +997,7 @@ expert_decode_kernel(ExpertArgs a) {
       for (int i2 = tid; i2 < T * kBRows; i2 += kWarps * 32) {
         const int t = i2 / kBRows, row = rb * kBRows + i2 % kBRows;
         unsigned long long v[kMaxTopK];
+        const float rv = a.res ? __ldg(a.res + (int64_t)t * H + row) : 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)  // all k reads in flight, waited on together, summed in j order
           if (j < k) v[j] = ld_relaxed_u64(a.obuf + (int64_t)(t * k + j) * H + row);
@@ -1003,7 +1006,9 @@ expert_decode_kernel(ExpertArgs a) {
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
           if (j < k) o += __uint_as_float((uint32_t)v[j]);
-        a.y[(int64_t)t * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        const uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        a.y[(int64_t)t * H + row] = yb;
+        if (a.res) a.ysum[(int64_t)t * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16f(yb) + rv));
       }
     }
   }
@@ -1027,7 +1032,7 @@ cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream
 }  // namespace
 
 cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
-                                cudaStream_t s, const moe_routing_out* dbg) {
+                                cudaStream_t s, const moe_routing_out* dbg, const float* res, uint16_t* ysum) {
   const moe_plan_desc& d = p.d;
   const int E = d.num_experts, H = d.hidden, I = d.inter, k = d.top_k, G = d.group_size;
   const int64_t ge0 = (int64_t)layer * E;
@@ -1122,6 +1127,8 @@ cudaError_t moe::decode_forward(Plan& p, int layer, const uint16_t* x, int T, ui
   a.tstride = std::min(d.max_tokens, kDecodeMaxTokens);
   a.obuf = p.obuf;
   a.y = y;
+  a.res = ysum ? res : nullptr;
+  a.ysum = ysum;
   for (int m = 0; m < 3; ++m) {
     a.m[m].codes = p.lay.m[m].codes_off;
     a.m[m].scales = p.lay.m[m].scales_off;

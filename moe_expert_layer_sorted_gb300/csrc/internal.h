@@ -178,14 +178,17 @@ cudaError_t launch_repack(const uint8_t* src_codes, const void* src_scales, uint
                           cudaStream_t s);
 cudaError_t launch_quantize(const float* w, int rows, int cols, int bits, int group, int sdt,
                             uint8_t* codes, void* scales, cudaStream_t s);
+// res / ysum (both or neither): also ysum = bf16(y + res), res fp32 [T][H]
 cudaError_t decode_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
-                           cudaStream_t s, const moe_routing_out* dbg);
+                           cudaStream_t s, const moe_routing_out* dbg, const float* res = nullptr,
+                           uint16_t* ysum = nullptr);
 cudaError_t lfu_step_end(Plan& p, cudaStream_t s);
 // lfu = false: the forward leaves the LFU state (counts, miss queue) as it is;
 // blob_hbm: the layer's HBM residence table to read (nullptr: the plan's own).
 cudaError_t prefill_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y, cudaStream_t s,
                             const moe_routing_out* dbg, bool lfu = true,
-                            const uint8_t* const* blob_hbm = nullptr);
+                            const uint8_t* const* blob_hbm = nullptr, const float* res = nullptr,
+                            uint16_t* ysum = nullptr);
 // Stages the layer's experts that are not in HBM into the prefill slots and
 // builds p.pf_blob (stream-ordered).
 cudaError_t prefill_stage(Plan& p, int layer, cudaStream_t s);

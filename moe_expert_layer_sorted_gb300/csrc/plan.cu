@@ -881,8 +881,15 @@ extern "C" moe_status moe_place_experts(moe_plan* plan, int layer, int first, in
   return st;
 }
 
-extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x, int T, void* y,
-                                        void* stream, const moe_routing_out* dbg) {
+namespace {
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+// moe_layer_forward, and with res / ysum (both non-NULL) the fused residual update
+moe_status layer_forward(moe_plan* plan, int layer, const void* x, int T, void* y, const float* res,
+                         void* ysum, void* stream, const moe_routing_out* dbg) {
   Plan* p = reinterpret_cast<Plan*>(plan);
   if (!p) return fail(nullptr, MOE_ERR_INVALID, "plan is NULL");
   Busy b(p);
@@ -894,6 +901,15 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
   if (!x || !y || x == y) return fail(p, MOE_ERR_INVALID, "x and y must be distinct non-NULL device buffers");
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 3))
     return fail(p, MOE_ERR_INVALID, "x must be 16-byte aligned and y 4-byte aligned");
+  if (ysum) {
+    const size_t nb = (size_t)T * d.hidden * 2;
+    if (!res) return fail(p, MOE_ERR_INVALID, "residual is NULL");
+    if ((reinterpret_cast<uintptr_t>(res) & 15) || (reinterpret_cast<uintptr_t>(ysum) & 15))
+      return fail(p, MOE_ERR_INVALID, "residual and out must be 16-byte aligned");
+    if (overlap(ysum, nb, x, nb) || overlap(ysum, nb, y, nb) || overlap(ysum, nb, res, 2 * nb) ||
+        overlap(res, 2 * nb, y, nb))
+      return fail(p, MOE_ERR_INVALID, "out must not overlap x, y or residual, nor residual y");
+  }
   const int64_t base = (int64_t)layer * d.num_experts;
   for (int e = 0; e < d.num_experts; ++e)
     if (!p->placed[base + e]) return fail(p, MOE_ERR_STATE, "every expert of the layer must be placed first");
@@ -915,11 +931,26 @@ extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x
   bool capturing = false;
   CK(p, order_before(p, s, capturing));
   cudaError_t e;
-  if (T <= kDecodeMaxTokens) e = decode_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
-  else e = prefill_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg);
+  if (T <= kDecodeMaxTokens)
+    e = decode_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg, res, (uint16_t*)ysum);
+  else
+    e = prefill_forward(*p, layer, (const uint16_t*)x, T, (uint16_t*)y, s, dbg, true, nullptr, res,
+                        (uint16_t*)ysum);
   if (e != cudaSuccess) return forward_fail(p, e, "forward launch");
   CK(p, order_after(p, s, capturing));
   return MOE_OK;
+}
+}  // namespace
+
+extern "C" moe_status moe_layer_forward(moe_plan* plan, int layer, const void* x, int T, void* y,
+                                        void* stream, const moe_routing_out* dbg) {
+  return layer_forward(plan, layer, x, T, y, nullptr, nullptr, stream, dbg);
+}
+
+extern "C" moe_status moe_layer_forward_residual(moe_plan* plan, int layer, const void* x, int T, void* y,
+                                                 const float* residual, void* out, void* stream) {
+  if (T > 0 && !out) return fail(reinterpret_cast<Plan*>(plan), MOE_ERR_INVALID, "out is NULL");
+  return layer_forward(plan, layer, x, T, y, residual, out, stream, nullptr);
 }
 
 extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void* x, int64_t T, void* y,

@@ -1287,9 +1287,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) pf_gemm_kernel(const __grid_c
 }
 
 // y[t][c] = sum over j ascending of o[inv[t*k + j]][c] (bf16 slot outputs, fp32 sum);
-// 8 columns per thread, the k slot rows' 16-byte pieces all requested before the sum
+// 8 columns per thread, the k slot rows' 16-byte pieces all requested before the sum.
+// With res != nullptr also ysum[t][c] = bf16(y[t][c] + res[t][c]) (the residual
+// update, res fp32; res and ysum 16-byte aligned).
 __global__ void pf_combine_kernel(const uint16_t* __restrict__ o, const int32_t* __restrict__ inv, int T,
-                                  int H, int k, uint16_t* __restrict__ y) {
+                                  int H, int k, uint16_t* __restrict__ y, const float* __restrict__ res,
+                                  uint16_t* __restrict__ ysum) {
   const int per = H / 8;
   const int64_t n = (int64_t)T * per;
   const bool y16 = (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
@@ -1321,6 +1324,16 @@ __global__ void pf_combine_kernel(const uint16_t* __restrict__ o, const int32_t*
     } else {  // y need only be 4-byte aligned
 #pragma unroll
       for (int q = 0; q < 4; ++q) reinterpret_cast<uint32_t*>(y)[4 * i + q] = out[q];
+    }
+    if (res) {
+      const float4 r0 = reinterpret_cast<const float4*>(res)[2 * i], r1 = reinterpret_cast<const float4*>(res)[2 * i + 1];
+      const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+      uint32_t so[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        so[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(bf16f(out[q] & 0xffffu) + rv[2 * q])) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(bf16f(out[q] >> 16) + rv[2 * q + 1])) << 16);
+      reinterpret_cast<uint4*>(ysum)[i] = make_uint4(so[0], so[1], so[2], so[3]);
     }
   }
 }
@@ -1446,7 +1459,7 @@ cudaError_t moe::router_norms(const uint16_t* wr, int E, int H, float* out, cuda
 
 cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, uint16_t* y,
                                  cudaStream_t s, const moe_routing_out* dbg, bool lfu,
-                                 const uint8_t* const* blob_hbm) {
+                                 const uint8_t* const* blob_hbm, const float* res, uint16_t* ysum) {
   const moe_plan_desc& d = p.d;
   const int E = d.num_experts, H = d.hidden, I = d.inter, k = d.top_k;
   const int n = T * k;
@@ -1545,7 +1558,7 @@ cudaError_t moe::prefill_forward(Plan& p, int layer, const uint16_t* x, int T, u
     if ((e = rows_map(&map, p.pf_h, n, I)) != cudaSuccess) return e;
     if ((e = launch_gemm<false>(d.weight_bits, map, a, p.sms, smem, s)) != cudaSuccess) return e;
   }
-  pf_combine_kernel<<<4 * p.sms, 256, 0, s>>>(p.pf_o, p.inv, T, H, k, y);
+  pf_combine_kernel<<<4 * p.sms, 256, 0, s>>>(p.pf_o, p.inv, T, H, k, y, res, ysum);
   pf_stats_kernel<<<1, 512, 0, s>>>(p.counts, E, bhbm, st,
                                     p.lay.algo_bytes, (int64_t)E * H * 2, n,
                                     lfu && d.cache_policy == MOE_POLICY_LFU, ge0, p.lfu_count, p.lfu_last,

@@ -60,9 +60,8 @@ def test_stack40_full_size(stack, T, layers):
     def body():
         xs[0].view(torch.int16).copy_(x0)
         for l in range(L):
-            plan.forward(l, xs[l], ys[l], stream=torch.cuda.current_stream())
-            synth.residual_bf16_device(ys[l].data_ptr(), noise[l].data_ptr(), T * H, xs[l + 1].data_ptr(),
-                                       torch.cuda.current_stream().cuda_stream)
+            # the layer's output and the next layer's input bf16(y_l + noise_l) in one forward
+            plan.forward_residual(l, xs[l], ys[l], noise[l], xs[l + 1], stream=torch.cuda.current_stream())
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
