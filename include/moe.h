@@ -232,7 +232,10 @@ moe_status moe_prefill_forward(moe_plan* plan, int layer, const void* x_bf16, in
 /* Same layer forward with HOST buffers: copies x (host [T][H] bf16) into the
  * plan's device staging buffer, runs the forward and copies y back into
  * y_host, all in stream order; the caller synchronises the stream before
- * reading y_host.  Pinned host buffers give asynchronous copies. */
+ * reading y_host.  Pinned host buffers give asynchronous copies.  For a
+ * decode-sized batch (T <= 8) in page-locked buffers (x_host 16-byte and
+ * y_host 4-byte aligned) no copy engine is used: a copy kernel reads x_host
+ * through its device mapping and the forward writes y_host through its own. */
 moe_status moe_layer_forward_host(moe_plan* plan, int layer, const void* x_host, int T,
                                   void* y_host, void* stream);
 

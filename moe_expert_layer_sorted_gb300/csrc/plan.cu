@@ -300,6 +300,13 @@ __global__ void quantize_kernel(const float* __restrict__ w, int rows, int cols,
   }
 }
 
+// dst[i] = src[i] for n16 16-byte words, one per thread (src: the device
+// mapping of a page-locked host buffer)
+__global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int n16) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n16) dst[i] = src[i];
+}
+
 // Streaming read of n16 16-byte words; the XOR of everything goes to *sink so
 // the loads cannot be removed.
 __global__ void read_probe_kernel(const uint4* __restrict__ p, int64_t n16, unsigned* sink) {
@@ -997,6 +1004,18 @@ extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void*
   return MOE_OK;
 }
 
+namespace {
+// The device address of a page-locked host buffer (nullptr for pageable memory)
+void* device_mapping(const void* h) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+}  // namespace
+
 extern "C" moe_status moe_layer_forward_host(moe_plan* plan, int layer, const void* x_host, int T,
                                              void* y_host, void* stream) {
   Plan* p = reinterpret_cast<Plan*>(plan);
@@ -1005,6 +1024,24 @@ extern "C" moe_status moe_layer_forward_host(moe_plan* plan, int layer, const vo
   if (T == 0) return MOE_OK;
   if (!x_host || !y_host) return fail(p, MOE_ERR_INVALID, "NULL host buffer");
   const size_t bytes = (size_t)T * p->d.hidden * 2;
+  if (T <= kDecodeMaxTokens) {
+    // Page-locked buffers of a decode-sized batch: x comes in by a copy kernel
+    // through its device mapping and the forward's combine writes y straight
+    // into y_host's (a copy-engine operation costs ~7.6 us of stream latency
+    // at these sizes, the kernel ~4.1 us, the direct writes nothing extra).
+    const void* xd = device_mapping(x_host);
+    void* yd = device_mapping(y_host);
+    if (xd && yd && !(reinterpret_cast<uintptr_t>(xd) & 15) && !(reinterpret_cast<uintptr_t>(yd) & 3)) {
+      const int n16 = (int)(bytes / 16);
+      {
+        DeviceScope ds(p->d.device);
+        copy16_kernel<<<(n16 + 255) / 256, 256, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(xd),
+                                                                          reinterpret_cast<uint4*>(p->x_stage), n16);
+        CK(p, cudaGetLastError());
+      }
+      return moe_layer_forward(plan, layer, p->x_stage, T, yd, stream, nullptr);
+    }
+  }
   {
     DeviceScope ds(p->d.device);
     CK(p, cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream));

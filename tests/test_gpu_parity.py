@@ -103,13 +103,31 @@ def test_empty_batch_is_a_noop(tiny):
     plan.forward(0, x, torch.empty_like(x))
 
 
-def test_host_buffer_forward_matches_device_forward(tiny):
+@pytest.mark.parametrize("T,mode", [(1, "pinned"), (8, "pinned"), (8, "pageable"), (5, "pinned-x-offset"),
+                                    (5, "pinned-y-offset")])
+def test_host_buffer_forward_matches_device_forward(tiny, T, mode):
+    """Host buffers give the device forward's bits: page-locked ones through
+    their device mappings (copy kernel in, direct writes out), pageable or
+    misaligned ones through copy-engine copies."""
     torch = _torch()
     wl, plan, info, _ = tiny
-    x = W.tokens(wl, 7, 0, 8)
+    H = wl.hidden
+    x = W.tokens(wl, 7 + T, 0, T)
     y_dev, _ = _run(plan, 0, x, wl)
-    xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
+    xs = torch.from_numpy(x.view(np.int16).copy())
+    if mode == "pageable":
+        xh, yh = xs.clone(), torch.zeros(T, H, dtype=torch.int16)
+    elif mode == "pinned-x-offset":  # x 8 bytes past a 16-byte boundary
+        buf = torch.zeros(T * H + 8, dtype=torch.int16).pin_memory()
+        xh = buf[4:4 + T * H].view(T, H)
+        xh.copy_(xs)
+        yh = torch.zeros(T, H, dtype=torch.int16).pin_memory()
+    elif mode == "pinned-y-offset":  # y 2 bytes past a 4-byte boundary
+        xh = xs.pin_memory()
+        buf = torch.zeros(T * H + 8, dtype=torch.int16).pin_memory()
+        yh = buf[1:1 + T * H].view(T, H)
+    else:
+        xh, yh = xs.pin_memory(), torch.zeros(T, H, dtype=torch.int16).pin_memory()
     plan.forward_host(0, xh, yh)
     torch.cuda.synchronize()
     assert torch.equal(yh, y_dev.view(torch.int16).cpu())

@@ -136,6 +136,24 @@ def test_prefill_output_4byte_aligned():
     plan.close()
 
 
+def test_prefill_host_buffer_forward():
+    """T > 8 with page-locked host buffers (copy-engine copies) gives the
+    device forward's bits."""
+    import torch
+    from moe_expert_layer_sorted_gb300 import harness
+    wl, T = MID, 300
+    plan, info = harness.build_plan(wl, max_tokens=T)
+    xs = torch.from_numpy(W.tokens(wl, 12, 0, T).view(np.int16).copy())
+    x = xs.cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    plan.forward(0, x, y)
+    xh, yh = xs.pin_memory(), torch.zeros(T, wl.hidden, dtype=torch.int16).pin_memory()
+    plan.forward_host(0, xh, yh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y.view(torch.int16).cpu())
+    plan.close()
+
+
 MIDH = W.Workload("prefill-mid-host", 1, 8, 512, 256, 2, (300,), 4, 64, W.SC_F32, "zipf", 1.0, host_total=4)
 MID3H = W.Workload("prefill-mid3-host", 1, 12, 512, 256, 3, (700,), 3, 128, W.SC_BF16, "zipf", 1.0,
                    host_total=7)
