@@ -1005,14 +1005,16 @@ extern "C" moe_status moe_prefill_forward(moe_plan* plan, int layer, const void*
 }
 
 namespace {
-// The device address of a page-locked host buffer (nullptr for pageable memory)
-void* device_mapping(const void* h) {
+// The address through which `device` reaches a page-locked host buffer that
+// was allocated or registered for it (nullptr otherwise: pageable memory, or
+// another device's)
+void* device_mapping(const void* h, int device) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+  return at.type == cudaMemoryTypeHost && at.device == device ? at.devicePointer : nullptr;
 }
 }  // namespace
 
@@ -1029,8 +1031,8 @@ extern "C" moe_status moe_layer_forward_host(moe_plan* plan, int layer, const vo
     // through its device mapping and the forward's combine writes y straight
     // into y_host's (a copy-engine operation costs ~7.6 us of stream latency
     // at these sizes, the kernel ~4.1 us, the direct writes nothing extra).
-    const void* xd = device_mapping(x_host);
-    void* yd = device_mapping(y_host);
+    const void* xd = device_mapping(x_host, p->d.device);
+    void* yd = device_mapping(y_host, p->d.device);
     if (xd && yd && !(reinterpret_cast<uintptr_t>(xd) & 15) && !(reinterpret_cast<uintptr_t>(yd) & 3)) {
       const int n16 = (int)(bytes / 16);
       {
