@@ -63,6 +63,8 @@ def test_bad_descriptors_rejected_on_the_host():
     assert L.moe_update_router_biases(None, 0, 1, None, None) == 1
     assert L.moe_debug_fail_next_forward(None) == 1
     assert L.moe_quantize(None, 4, 4, 4, 4, 0, None, None, None) == 1
+    assert L.moe_layer_forward_residual(None, 0, None, 1, None, None, None, None) == 1
+    assert L.moe_layer_forward_host(None, 0, None, 1, None, None) == 1
 
 
 def test_no_device_is_an_error_not_a_crash():
